@@ -1,0 +1,351 @@
+"""Plain fp64 CPU oracle for MC-Sparse token-sparse attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links
+this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it.  It shares no code with the CUDA library.
+
+Every function works on ONE attention head at a time (arrays ``[N, D]``), in
+float64, on inputs that are already bf16 values (the bytes the GPU receives).
+The arithmetic follows the method step by step, in the order the pages give it;
+library primitives (matmul, exp, sort) serve as single steps and nothing is
+blocked, fused or reordered.
+
+Sources.  All pages carry the title "MC-Sparse: Deconstructing and Closing the
+Dense-Sparse Attention Gap in Diffusion Transformers".  Citations below name
+the site and the section:
+
+* [ai.info/Method]  ai.info AI summary, section "Methodology in Plain English".
+* [ai.info/Contrib] ai.info AI summary, section "Key Contributions".
+* [wisp/Tile]       wispaper.ai, section "Token-level selection needs
+                    tile-aligned query groups".
+* [wisp/Reuse]      wispaper.ai, section "Reused exact selection beats
+                    recomputed mean pooling".
+* [wisp/Residual]   wispaper.ai, section "Residual correction recovers the
+                    discarded tail".
+* [wisp/Gap]        wispaper.ai, section "The gap has three separable sources".
+* [agihunt/Select]  agihunt.info summary, paragraph on the selection objective
+                    (top-K KV tokens of largest group attention mass, two-pass
+                    kernel).
+* [agihunt/Group]   agihunt.info summary, paragraph on token-level gathering
+                    and PDDP groups of exactly C queries.
+
+Readings taken where the pages are silent (each repeated at its function):
+softmax scale 1/sqrt(D); natural-log LSE; PDDP centred covariance, power
+iteration from (1,..,1)/sqrt(D) for ``iters`` steps, sign fixed by the largest
+|component| (lowest index on ties); median split at rank C*floor(g/2) with ties
+broken by token index; leaves in tree order (left first), ascending inside a
+leaf, the one short leaf (when C does not divide N) last and padded with -1;
+top-K ties to the lower KV index, result ascending; sparse softmax
+renormalised over the selected K only; the residual is taken against the
+stored bf16 dense output and stored as bf16.
+
+Parity status: every function here is pinned by tests in
+``tests/test_oracle_pins.py`` (closed forms, library routines, brute force,
+invariants); none is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "round_to_bf16",
+    "default_scale",
+    "dense_attention",
+    "principal_direction",
+    "pddp_leaves",
+    "pddp_perm",
+    "group_members",
+    "group_mass",
+    "topk_select",
+    "per_query_topk_mass",
+    "sparse_attention",
+    "sparse_attention_group",
+    "anchor_step",
+    "reuse_step",
+]
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage rounding
+# ---------------------------------------------------------------------------
+
+def round_to_bf16(x) -> np.ndarray:
+    """Round real values to the nearest bfloat16 (ties to even), as float64.
+
+    bfloat16 keeps 8 significant bits and the float32 exponent range.  For
+    x = m * 2**e with 0.5 <= |m| < 1 the spacing of bf16 values around x is
+    2**(e-8); below the smallest normal (e < -125) the spacing stays 2**-133.
+    ``np.rint`` rounds half-way cases to even.  Values beyond the bf16 range do
+    not occur here and are not handled.
+    """
+    a = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(a)
+    e = np.maximum(e, -125)
+    ulp = np.ldexp(1.0, e - 8)
+    return np.rint(a / ulp) * ulp
+
+
+def default_scale(D: int) -> float:
+    """Softmax temperature.  The pages do not state it; standard attention
+    uses 1/sqrt(D), and that is the reading taken."""
+    return 1.0 / math.sqrt(D)
+
+
+# ---------------------------------------------------------------------------
+# a2: dense attention with log-sum-exp  [ai.info/Method], [agihunt/Select]
+# ---------------------------------------------------------------------------
+
+def dense_attention(q, k, v, scale, rows=None):
+    """Dense softmax attention of one head, plus the per-query log-sum-exp.
+
+    The selector's first pass "computes the dense output and row-wise
+    log-sum-exp values" [ai.info/Method].  With S = scale * q k^T:
+        lse_i = log sum_j exp(S_ij)            (natural log; reading)
+        O_i   = sum_j exp(S_ij - lse_i) v_j
+    ``rows`` restricts the computation to some query rows (each row is
+    independent of the others).  Returns (O [r, D], lse [r]).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    if rows is not None:
+        q = q[np.asarray(rows)]
+    S = scale * (q @ k.T)
+    m = S.max(axis=1)
+    lse = m + np.log(np.exp(S - m[:, None]).sum(axis=1))
+    P = np.exp(S - lse[:, None])
+    return P @ v, lse
+
+
+# ---------------------------------------------------------------------------
+# a1: Fast PDDP median-split grouping  [wisp/Tile], [ai.info/Method],
+#     [ai.info/Contrib], [agihunt/Group]
+# ---------------------------------------------------------------------------
+
+def principal_direction(cov, iters: int):
+    """Leading eigenvector of a covariance matrix by power iteration.
+
+    The pages name batched power iteration as the way the principal direction
+    is found [ai.info/Contrib]; start vector, step count and sign are not
+    given.  Reading: start at (1,...,1)/sqrt(D), apply v <- Cv/|Cv| ``iters``
+    times (stop early only if Cv is exactly zero, i.e. a degenerate node),
+    then flip the sign so that the component of largest magnitude is
+    positive (the lowest such index on ties).
+    """
+    cov = np.asarray(cov, np.float64)
+    D = cov.shape[0]
+    v = np.full(D, 1.0 / math.sqrt(D))
+    for _ in range(iters):
+        w = cov @ v
+        norm = math.sqrt(float(w @ w))
+        if norm == 0.0:
+            break
+        v = w / norm
+    lead = int(np.argmax(np.abs(v)))  # argmax returns the first maximum
+    if v[lead] < 0:
+        v = -v
+    return v
+
+
+def pddp_leaves(x, C: int, iters: int = 32):
+    """Median-split principal direction divisive partitioning of one head.
+
+    Each node is projected onto its principal direction and the ordered
+    queries are split at the median, recursively, until every group holds C
+    queries [wisp/Tile], [agihunt/Group].  The pages assume C divides the
+    node; for a node of n rows, g = ceil(n / C) groups, the reading taken is:
+    the left child receives the C*floor(g/2) rows of smallest projection and
+    the right child the rest, so the only short group is the right-most leaf.
+
+    Per node: mu = mean, Cov = sum_i (x_i - mu)(x_i - mu)^T, v = leading
+    direction (``principal_direction``), t_i = (x_i - mu).v, order rows by
+    (t_i, token index) ascending, split, recurse left then right.
+
+    Returns the leaves left to right, each an ascending int64 array of token
+    indices.
+    """
+    x = np.asarray(x, np.float64)
+    N = x.shape[0]
+    leaves = []
+
+    def split(members):
+        n = members.shape[0]
+        g = -(-n // C)
+        if g <= 1:
+            leaves.append(np.sort(members))
+            return
+        xs = x[members]
+        mu = xs.mean(axis=0)
+        xc = xs - mu
+        cov = xc.T @ xc
+        v = principal_direction(cov, iters)
+        t = xc @ v
+        order = np.lexsort((members, t))  # primary key t, then token index
+        n_left = C * (g // 2)
+        split(members[order[:n_left]])
+        split(members[order[n_left:]])
+
+    split(np.arange(N, dtype=np.int64))
+    return leaves
+
+
+def pddp_perm(x, C: int, iters: int = 32):
+    """PDDP groups as the padded permutation array ``[G*C]`` (int64).
+
+    Group g occupies positions [g*C, (g+1)*C); entry p holds the original
+    token index at that position; unused slots of the short last group are
+    -1.  G = ceil(N / C).
+    """
+    N = np.asarray(x).shape[0]
+    G = -(-N // C)
+    perm = np.full(G * C, -1, dtype=np.int64)
+    for g, leaf in enumerate(pddp_leaves(x, C, iters)):
+        perm[g * C: g * C + leaf.shape[0]] = leaf
+    return perm
+
+
+def group_members(perm, g: int, C: int):
+    """Token indices of group g in a padded permutation (padding dropped)."""
+    seg = np.asarray(perm)[g * C:(g + 1) * C]
+    return seg[seg >= 0]
+
+
+# ---------------------------------------------------------------------------
+# a3 + a4: exact group mass and top-K  [agihunt/Select], [ai.info/Method]
+# ---------------------------------------------------------------------------
+
+def group_mass(q, k, lse, members, scale):
+    """Attention mass a query group puts on every KV token.
+
+    The second selector pass recomputes QK scores and recovers the exact
+    attention probabilities from the first pass's LSE [ai.info/Method]:
+        P_ij = exp(scale * q_i.k_j - lse_i)        (full-row softmax)
+        mass[j] = sum_{i in group} P_ij
+    Returns mass over all N KV tokens.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    lse = np.asarray(lse, np.float64)
+    members = np.asarray(members)
+    S = scale * (q[members] @ k.T)
+    return np.exp(S - lse[members][:, None]).sum(axis=0)
+
+
+def topk_select(mass, K: int):
+    """The K KV tokens of largest group mass, returned ascending.
+
+    The objective is the K KV tokens whose summed group attention weight is
+    largest [agihunt/Select].  Ties (equal mass) go to the lower token index
+    (reading).  Returns (idx ascending int64 [K], retained mass = sum of the
+    selected masses).
+    """
+    mass = np.asarray(mass, np.float64)
+    n = mass.shape[0]
+    order = np.lexsort((np.arange(n), -mass))  # mass descending, then index
+    idx = np.sort(order[:K])
+    return idx, float(mass[idx].sum())
+
+
+def per_query_topk_mass(q, k, lse, rows, K: int, scale):
+    """The per-query oracle: each query keeps its own K most probable KV
+    tokens; returns the kept probability mass per query.  Summed over a group
+    it bounds from above what any shared selection of K tokens can retain
+    [wisp/Gap], [ai.info/Method]."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    lse = np.asarray(lse, np.float64)
+    rows = np.asarray(rows)
+    P = np.exp(scale * (q[rows] @ k.T) - lse[rows][:, None])
+    P.sort(axis=1)
+    return P[:, -K:].sum(axis=1)
+
+
+# ---------------------------------------------------------------------------
+# a5: token-sparse attention  [wisp/Tile], [ai.info/Method], [agihunt/Group]
+# ---------------------------------------------------------------------------
+
+def sparse_attention_group(q, k, v, members, idx, scale):
+    """Attention of one query group restricted to its selected KV tokens.
+
+    The group's queries attend only to the gathered rows idx of K and V
+    [wisp/Tile]; the softmax is renormalised over those K tokens (reading:
+    the discarded tail is what the residual accounts for [wisp/Residual]).
+    Returns O' [|group|, D].
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    members = np.asarray(members)
+    idx = np.asarray(idx)
+    S = scale * (q[members] @ k[idx].T)
+    m = S.max(axis=1)
+    P = np.exp(S - m[:, None])
+    P /= P.sum(axis=1)[:, None]
+    return P @ v[idx]
+
+
+def sparse_attention(q, k, v, perm, idx, C: int, scale, groups=None):
+    """Token-sparse attention of one head, in original token order.
+
+    ``idx`` is ``[G, K]``.  Rows of tokens outside the requested ``groups``
+    are left as NaN.  Returns O' [N, D].
+    """
+    q = np.asarray(q, np.float64)
+    N, D = q.shape
+    idx = np.asarray(idx)
+    G = idx.shape[0]
+    out = np.full((N, np.asarray(v).shape[1]), np.nan)
+    for g in (range(G) if groups is None else groups):
+        members = group_members(perm, g, C)
+        if members.shape[0]:
+            out[members] = sparse_attention_group(q, k, v, members, idx[g], scale)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Anchor and reuse steps  [wisp/Reuse], [wisp/Residual]
+# ---------------------------------------------------------------------------
+
+def anchor_step(q, k, v, C: int, K: int, scale, iters: int = 32):
+    """Everything one anchor step computes for one head.
+
+    At an anchor the method groups the queries, selects KV tokens with exact
+    probabilities, outputs dense attention, and records the residual between
+    the dense and the sparse outputs [wisp/Reuse], [wisp/Residual].  Data
+    flow (reading): the dense output is stored as bf16; the residual is
+    ``bf16(dense_bf16 - O')`` with O' the sparse output under the new groups
+    and indices.
+
+    Returns a dict with perm [G*C], lse [N], dense (fp64), dense_bf16,
+    mass [G, N], idx [G, K], retained [G], sparse (fp64 O'), residual (bf16
+    values).
+    """
+    q = np.asarray(q, np.float64)
+    N = q.shape[0]
+    G = -(-N // C)
+    perm = pddp_perm(q, C, iters)
+    dense, lse = dense_attention(q, k, v, scale)
+    mass = np.empty((G, N))
+    idx = np.empty((G, K), dtype=np.int64)
+    retained = np.empty(G)
+    for g in range(G):
+        mass[g] = group_mass(q, k, lse, group_members(perm, g, C), scale)
+        idx[g], retained[g] = topk_select(mass[g], K)
+    sparse = sparse_attention(q, k, v, perm, idx, C, scale)
+    dense_bf16 = round_to_bf16(dense)
+    residual = round_to_bf16(dense_bf16 - sparse)
+    return dict(perm=perm, lse=lse, dense=dense, dense_bf16=dense_bf16,
+                mass=mass, idx=idx, retained=retained, sparse=sparse,
+                residual=residual)
+
+
+def reuse_step(q, k, v, perm, idx, residual, C: int, scale):
+    """Output of a reuse step for one head: the current step's sparse
+    attention under the cached groups and indices, plus the cached residual
+    [wisp/Residual].  Returns the exact (fp64) sum; the stored output is its
+    bf16 rounding."""
+    sparse = sparse_attention(q, k, v, perm, idx, C, scale)
+    return sparse + np.asarray(residual, np.float64)

@@ -1,0 +1,290 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test ties one oracle function to a textbook or library routine, a closed
+form, a hand-worked fixture (tests/golden), brute force or an invariant the
+method fixes, chosen so that a plausible slip (a dropped term, a wrong sign or
+index, a transposed operand) fails at least one of them.  CPU only.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mcs_oracle as orc
+from tests.parity import separated_clusters
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def _bf16(a):
+    return orc.round_to_bf16(a)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_rounding_matches_torch():
+    rng = _rng(1)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+        (rng.standard_normal(2000) * 1e4).astype(np.float32),
+        # exact half-way cases: bf16 value + half an ulp, both parities
+        np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(2.0 + 2.0 ** -7), 0.0], np.float32),
+    ])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.round_to_bf16(x.astype(np.float64)), want)
+
+
+# ---------------------------------------------------------------- dense + LSE
+
+@pytest.mark.parametrize("N,D", [(37, 16), (128, 64), (200, 128)])
+def test_dense_matches_torch_sdpa(N, D):
+    rng = _rng(N)
+    q, k, v = (_bf16(rng.standard_normal((N, D)) * s) for s in (2.0, 1.0, 1.0))
+    scale = orc.default_scale(D)
+    O, lse = orc.dense_attention(q, k, v, scale)
+    tq, tk, tv = (torch.from_numpy(a)[None, None] for a in (q, k, v))
+    want = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)[0, 0]
+    np.testing.assert_allclose(O, want.numpy(), rtol=1e-10, atol=1e-12)
+    S = torch.from_numpy(q) @ torch.from_numpy(k).T * scale
+    np.testing.assert_allclose(lse, torch.logsumexp(S, dim=1).numpy(), rtol=1e-12)
+
+
+def test_dense_lse_bounds_and_rows_sum_to_one():
+    rng = _rng(3)
+    N, D = 150, 32
+    q, k, v = (rng.standard_normal((N, D)) for _ in range(3))
+    scale = 0.7
+    _, lse = orc.dense_attention(q, k, v, scale)
+    S = scale * q @ k.T
+    assert np.all(lse >= S.max(1) - 1e-12)
+    assert np.all(lse <= S.max(1) + math.log(N) + 1e-12)
+    np.testing.assert_allclose(np.exp(S - lse[:, None]).sum(1), 1.0, rtol=1e-12)
+
+
+def test_dense_closed_form_identical_keys():
+    # every key equal -> every score in a row equal -> uniform weights:
+    # O_i = mean of V rows, lse_i = s_i + log N
+    rng = _rng(4)
+    N, D = 64, 16
+    q = rng.standard_normal((N, D))
+    k = np.tile(rng.standard_normal(D), (N, 1))
+    v = rng.standard_normal((N, D))
+    O, lse = orc.dense_attention(q, k, v, 0.5)
+    np.testing.assert_allclose(O, np.tile(v.mean(0), (N, 1)), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, 0.5 * q @ k[0] + math.log(N), rtol=1e-12)
+
+
+def test_dense_rows_subset_equals_full():
+    rng = _rng(5)
+    q, k, v = (rng.standard_normal((90, 8)) for _ in range(3))
+    O, lse = orc.dense_attention(q, k, v, 0.3)
+    rows = np.array([0, 17, 89])
+    O2, lse2 = orc.dense_attention(q, k, v, 0.3, rows=rows)
+    np.testing.assert_array_equal(O2, O[rows])
+    np.testing.assert_array_equal(lse2, lse[rows])
+
+
+# ---------------------------------------------------------------- power iteration
+
+def test_principal_direction_matches_eigh():
+    rng = _rng(6)
+    D = 24
+    Q, _ = np.linalg.qr(rng.standard_normal((D, D)))
+    evals = np.concatenate([[20.0, 6.0], rng.uniform(0.1, 5.0, D - 2)])
+    cov = (Q * evals) @ Q.T
+    v = orc.principal_direction(cov, 64)
+    w, U = np.linalg.eigh(cov)
+    u = U[:, -1]
+    lead = int(np.argmax(np.abs(u)))
+    u = u if u[lead] > 0 else -u
+    np.testing.assert_allclose(v, u, atol=1e-8)
+    assert v[np.argmax(np.abs(v))] > 0
+
+
+def test_principal_direction_sign_rule_and_degenerate():
+    # rank one along u whose largest component is negative -> result is -u/|u|
+    u = np.array([0.1, -3.0, 0.5, 1.0])
+    v = orc.principal_direction(np.outer(u, u), 5)
+    np.testing.assert_allclose(v, -u / np.linalg.norm(u), atol=1e-14)
+    # zero covariance: the start vector is kept
+    v0 = orc.principal_direction(np.zeros((4, 4)), 5)
+    np.testing.assert_allclose(v0, np.full(4, 0.5))
+
+
+# ---------------------------------------------------------------- PDDP
+
+def _check_valid_perm(perm, N, C):
+    G = -(-N // C)
+    assert perm.shape == (G * C,)
+    real = perm[perm >= 0]
+    assert np.array_equal(np.sort(real), np.arange(N))
+    for g in range(G):
+        seg = perm[g * C:(g + 1) * C]
+        n_real = int((seg >= 0).sum())
+        assert n_real == (C if g < G - 1 else N - (G - 1) * C)
+        assert np.all(seg[:n_real] >= 0) and np.all(seg[n_real:] == -1)
+        assert np.all(np.diff(seg[:n_real]) > 0)
+
+
+def test_pddp_golden_four_pairs():
+    fx = json.load(open(os.path.join(GOLDEN, "pddp_four_pairs.json")))
+    x = np.array(fx["points"])
+    perm = orc.pddp_perm(x, fx["C"], 32)
+    assert perm.tolist() == fx["expected_perm"]
+
+
+@pytest.mark.parametrize("N,C", [(256, 32), (300, 32), (1000, 64), (97, 16)])
+def test_pddp_on_a_line_is_sorting(N, C):
+    # x_i = t_i * u: every node's covariance has rank one along u, so each split
+    # orders by t (u's largest component is positive) and the leaves are
+    # consecutive C-chunks of the order by (t, index).
+    rng = _rng(N + C)
+    D = 8
+    u = rng.standard_normal(D)
+    u[np.argmax(np.abs(u))] = abs(u[np.argmax(np.abs(u))]) + 1.0
+    t = rng.standard_normal(N)
+    t[::7] = t[3]  # some exact ties, broken by token index
+    x = np.outer(t, u)
+    perm = orc.pddp_perm(x, C, 32)
+    order = np.lexsort((np.arange(N), t))
+    G = -(-N // C)
+    want = np.full(G * C, -1)
+    for g in range(G):
+        chunk = np.sort(order[g * C:(g + 1) * C])
+        want[g * C:g * C + chunk.shape[0]] = chunk
+    np.testing.assert_array_equal(perm, want)
+
+
+@pytest.mark.parametrize("N,C,D", [(512, 64, 16), (2048, 64, 128), (1000, 128, 64), (3000, 128, 128)])
+def test_pddp_recovers_separated_clusters(N, C, D):
+    x, want = separated_clusters(N, C, D, seed=N + D)
+    np.testing.assert_array_equal(orc.pddp_perm(x, C, 32), want)
+
+
+def test_pddp_valid_and_translation_invariant():
+    rng = _rng(8)
+    N, C, D = 777, 32, 12
+    x = rng.standard_normal((N, D)) * rng.uniform(0.5, 2.0, D)
+    perm = orc.pddp_perm(x, C, 32)
+    _check_valid_perm(perm, N, C)
+    # centring: shifting every point by the same vector changes nothing
+    shifted = orc.pddp_perm(x + 50.0 * rng.standard_normal(D), C, 32)
+    np.testing.assert_array_equal(perm, shifted)
+
+
+# ---------------------------------------------------------------- group mass, top-K
+
+def _head(N, D, seed, qs=2.0):
+    rng = _rng(seed)
+    q, k, v = (_bf16(rng.standard_normal((N, D)) * s) for s in (qs, 1.0, 1.0))
+    return q, k, v
+
+
+def test_group_mass_matches_torch_softmax_and_sums_to_group_size():
+    N, D = 300, 32
+    q, k, _ = _head(N, D, 9)
+    scale = orc.default_scale(D)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    members = np.array([3, 50, 51, 199, 299])
+    mass = orc.group_mass(q, k, lse, members, scale)
+    P = torch.softmax(torch.from_numpy(q @ k.T * scale), dim=1).numpy()
+    np.testing.assert_allclose(mass, P[members].sum(0), rtol=1e-11, atol=1e-15)
+    assert math.isclose(mass.sum(), members.shape[0], rel_tol=1e-12)
+
+
+def test_topk_golden_ties():
+    fx = json.load(open(os.path.join(GOLDEN, "topk_ties.json")))
+    for case in fx["cases"]:
+        idx, kept = orc.topk_select(np.array(fx["mass"]), case["K"])
+        assert idx.tolist() == case["idx"]
+        assert math.isclose(kept, sum(fx["mass"][i] for i in case["idx"]))
+
+
+@pytest.mark.parametrize("n,K", [(8, 3), (12, 5), (10, 1), (9, 9)])
+def test_topk_brute_force(n, K):
+    mass = _rng(n * 10 + K).uniform(0, 1, n)
+    best = max(itertools.combinations(range(n), K), key=lambda s: sum(mass[list(s)]))
+    idx, kept = orc.topk_select(mass, K)
+    assert idx.tolist() == list(best)
+    assert math.isclose(kept, mass[list(best)].sum(), rel_tol=1e-14)
+
+
+def test_retained_mass_bounds():
+    N, D, C, K = 512, 32, 32, 60
+    q, k, _ = _head(N, D, 10)
+    scale = orc.default_scale(D)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    perm = orc.pddp_perm(q, C, 32)
+    rng = _rng(11)
+    for g in (0, 5, 15):
+        members = orc.group_members(perm, g, C)
+        mass = orc.group_mass(q, k, lse, members, scale)
+        idx, kept = orc.topk_select(mass, K)
+        # the per-query oracle is an upper bound for any shared selection
+        bound = orc.per_query_topk_mass(q, k, lse, members, K, scale).sum()
+        assert kept <= bound + 1e-12
+        # and the chosen set beats random sets of the same size
+        for _ in range(50):
+            other = rng.choice(N, size=K, replace=False)
+            assert kept >= mass[other].sum() - 1e-12
+
+
+# ---------------------------------------------------------------- sparse + residual
+
+def test_sparse_full_density_equals_dense():
+    N, D, C = 200, 32, 32
+    q, k, v = _head(N, D, 12)
+    scale = orc.default_scale(D)
+    perm = orc.pddp_perm(q, C, 32)
+    G = -(-N // C)
+    idx = np.tile(np.arange(N), (G, 1))
+    sparse = orc.sparse_attention(q, k, v, perm, idx, C, scale)
+    dense, _ = orc.dense_attention(q, k, v, scale)
+    np.testing.assert_allclose(sparse, dense, rtol=1e-11, atol=1e-13)
+
+
+def test_sparse_fixed_subset_equals_sdpa_on_subset():
+    N, D, C, K = 160, 16, 16, 23
+    q, k, v = _head(N, D, 13)
+    scale = orc.default_scale(D)
+    rng = _rng(14)
+    perm = np.concatenate([rng.permutation(N), np.full((-(-N // C)) * C - N, -1)])
+    perm = perm.reshape(-1, C)
+    perm = np.stack([np.concatenate([np.sort(r[r >= 0]), r[r < 0]]) for r in perm]).reshape(-1)
+    sub = np.sort(rng.choice(N, K, replace=False))
+    idx = np.tile(sub, (-(-N // C), 1))
+    sparse = orc.sparse_attention(q, k, v, perm, idx, C, scale)
+    want = torch.nn.functional.scaled_dot_product_attention(
+        *(torch.from_numpy(a)[None, None] for a in (q, k[sub], v[sub])), scale=scale)[0, 0]
+    np.testing.assert_allclose(sparse, want.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_anchor_identity_and_reuse_reproduces_dense():
+    N, D, C, K = 256, 32, 32, 40
+    q, k, v = _head(N, D, 15)
+    scale = orc.default_scale(D)
+    a = orc.anchor_step(q, k, v, C, K, scale)
+    _check_valid_perm(a["perm"], N, C)
+    # the residual is stored in bf16: sparse + R equals the stored dense output
+    # up to half a bf16 spacing of R
+    half_ulp_r = np.ldexp(1.0, np.frexp(a["residual"])[1] - 9)
+    assert np.all(np.abs(a["sparse"] + a["residual"] - a["dense_bf16"]) <= half_ulp_r + 1e-15)
+    # reuse with unchanged inputs gives the dense output back
+    out = orc.reuse_step(q, k, v, a["perm"], a["idx"], a["residual"], C, scale)
+    assert np.max(np.abs(out - a["dense"])) < 1e-2
+    assert np.max(np.abs(orc.round_to_bf16(out) - a["dense_bf16"])) <= np.max(np.abs(a["dense"])) * 2 ** -7
+    # the selection keeps most of the mass on these peaked inputs, never more than
+    # the group size
+    sizes = np.array([orc.group_members(a["perm"], g, C).shape[0] for g in range(a["idx"].shape[0])])
+    assert np.all(a["retained"] <= sizes + 1e-9)
+    np.testing.assert_allclose(a["mass"].sum(1), sizes, rtol=1e-12)
