@@ -1,0 +1,173 @@
+/*
+ * mcs.h -- C ABI of the MC-Sparse token-sparse attention library (libmcs.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Method: "MC-Sparse: Deconstructing and Closing the Dense-Sparse Attention
+ * Gap in Diffusion Transformers".  Each tile-aligned group of C similar
+ * queries of one head attends only to its own K selected KV tokens, gathered
+ * by index; groups, KV indices and the dense-minus-sparse residual are
+ * computed at anchor steps and reused at the reuse steps in between.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned DEVICE memory, contiguous, row-major:
+ *      q, k, v, out, dense_out, residual : [B, H, N, D] bfloat16
+ *      lse                               : [B, H, N]    float32 (natural log)
+ *      perm                              : [B, H, G*C]  int32, G = ceil(N/C)
+ *      idx                               : [B, H, G, K] int32
+ *      mass                              : [heads, G, N] float32
+ *    Pointers to bf16 tensors must be 16-byte aligned.
+ *  - perm: entry g*C + p is the original token index of query p of group g;
+ *    the unused slots of the short last group (when C does not divide N) are
+ *    -1.  Within a group indices are ascending.
+ *  - idx: the selected KV token indices of each group, ascending.
+ *  - Calls are asynchronous on `stream`; outputs are valid once the stream
+ *    has reached the call.  Arguments are checked on the host before any
+ *    launch; on a check failure nothing is launched and a status is returned.
+ *  - Faults found on the device (an index out of range, a bounded wait that
+ *    gave up) are OR-ed into a device status word read by mcs_device_status.
+ *    Kernels never trap.
+ *  - The library allocates no memory.  Entry points that need scratch take
+ *    a caller-provided device workspace (size from the *_workspace queries).
+ *    Apart from the device status word it holds no state between calls.
+ *  - Supported: D in {64, 128}, C in {64, 128}, 1 <= K <= N, B*H <= 65535.
+ */
+#ifndef MCS_H_
+#define MCS_H_
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MCS_OK = 0,
+  MCS_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  MCS_ERR_UNSUPPORTED = 2, /* D, C outside the supported set */
+  MCS_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  MCS_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (mcs_last_cuda_error) */
+  MCS_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up */
+  MCS_ERR_BOUNDS = 6       /* a perm/idx entry was outside [0, N) on the device */
+} mcs_status;
+
+typedef struct {
+  int B, H, N, D;  /* batch, heads, tokens per head, head dim */
+  int C;           /* queries per group (the kernel's query tile) */
+  int K;           /* selected KV tokens per group: round(density * N) */
+  float scale;     /* softmax scale; 0 selects 1/sqrt(D) */
+  int pddp_iters;  /* power-iteration steps per PDDP node; 0 selects 32 */
+} mcs_params;
+
+/* Human-readable name of a status code (static string). */
+const char* mcs_status_string(mcs_status s);
+
+/* Message of the last CUDA error seen by this thread (static per thread). */
+const char* mcs_last_cuda_error(void);
+
+/*
+ * Device status: synchronises `stream`, returns the first device-side fault
+ * recorded since the previous call (MCS_ERR_TIMEOUT, MCS_ERR_BOUNDS) or
+ * MCS_OK, and clears the word.
+ */
+mcs_status mcs_device_status(cudaStream_t stream);
+
+/* Workspace bytes needed by mcs_group and by mcs_anchor_select. */
+size_t mcs_group_workspace(const mcs_params* p);
+size_t mcs_anchor_workspace(const mcs_params* p);
+
+/*
+ * a1 -- Fast PDDP query grouping.  Source: wispaper.ai, "Token-level
+ * selection needs tile-aligned query groups" (median split along each
+ * group's principal direction until every group holds C queries); ai.info
+ * AI summary, "Methodology in Plain English" / "Key Contributions" (batched
+ * power iteration over all heads per tree depth, only index arrays passed
+ * between levels).
+ * Reads q [B,H,N,D]; writes perm [B,H,G*C].  For a node of n rows and
+ * g = ceil(n/C) groups, the left child takes the C*floor(g/2) rows of
+ * smallest projection (ties by token index); the principal direction is
+ * pddp_iters power-iteration steps from (1,...,1)/sqrt(D), sign fixed so its
+ * largest-magnitude component is positive.  Leaves in tree order, indices
+ * ascending within a group, the short group last.
+ * ws: device workspace of at least mcs_group_workspace(p) bytes.
+ */
+mcs_status mcs_group(const mcs_params* p, const void* q, int32_t* perm, void* ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
+ * a2 -- Dense attention with per-query log-sum-exp, the selector's first
+ * pass (ai.info AI summary, "Methodology in Plain English": "computes the
+ * dense output and row-wise log-sum-exp values") and the speedup baseline.
+ * out = softmax(scale * q k^T) v  [B,H,N,D] bf16;
+ * lse = log sum_j exp(scale * q_i.k_j)  [B,H,N] fp32, nullable.
+ */
+mcs_status mcs_dense_attn(const mcs_params* p, const void* q, const void* k, const void* v,
+                          void* out, float* lse, cudaStream_t stream);
+
+/*
+ * a3 -- Exact group attention mass, the selector's second pass (ai.info AI
+ * summary, "Methodology in Plain English"; agihunt.info summary, paragraph on
+ * the selection objective): for heads [head_begin, head_begin + head_count)
+ * (numbered b*H + h) and every group g,
+ *     mass[h - head_begin, g, j] = sum_{i in group g} exp(scale*q_i.k_j - lse_i).
+ * Padding slots (perm = -1) contribute nothing.  mass: [head_count, G, N] fp32.
+ */
+mcs_status mcs_group_mass(const mcs_params* p, const void* q, const void* k, const float* lse,
+                          const int32_t* perm, int head_begin, int head_count, float* mass,
+                          cudaStream_t stream);
+
+/*
+ * a4 -- Per-group top-K (agihunt.info summary, paragraph on the selection
+ * objective: the K KV tokens of largest group attention weight).  For each of
+ * `rows` rows of p->N non-negative masses, writes the K indices of largest
+ * mass (ties to the lower index) in ascending order to idx [rows, K] and,
+ * when `retained` is not NULL, the sum of their masses to retained [rows].
+ */
+mcs_status mcs_topk(const mcs_params* p, const float* mass, int rows, int32_t* idx,
+                    float* retained, cudaStream_t stream);
+
+/*
+ * a5 + a6 -- Token-sparse attention (wispaper.ai, "Token-level selection
+ * needs tile-aligned query groups"; "Residual correction recovers the
+ * discarded tail").  For every group g of every head: the group's queries
+ * attend to the K rows idx[b,h,g,:] of k and v only (softmax renormalised
+ * over those K), and the result of query row perm[g*C+p] is written to that
+ * row of out.  When `residual` is not NULL it is added (reuse step):
+ * out = O' + residual.
+ */
+mcs_status mcs_sparse_attn(const mcs_params* p, const void* q, const void* k, const void* v,
+                           const int32_t* perm, const int32_t* idx, const void* residual,
+                           void* out, cudaStream_t stream);
+
+/*
+ * Anchor form of a5 (wispaper.ai, "Residual correction recovers the
+ * discarded tail": recording the residual costs one sparse evaluation and
+ * an elementwise subtraction): residual = bf16(dense_out - O'), rows in
+ * original token order.
+ */
+mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void* k,
+                                  const void* v, const int32_t* perm, const int32_t* idx,
+                                  const void* dense_out, void* residual, cudaStream_t stream);
+
+/*
+ * The whole anchor step (wispaper.ai, "Reused exact selection beats
+ * recomputed mean pooling"; "Residual correction recovers the discarded
+ * tail"): a1 grouping -> perm; a2 dense attention -> dense_out (the step's
+ * output) and lse; a3 + a4 exact selection -> idx (and retained mass
+ * [B,H,G], nullable); a5 anchor form -> residual.
+ * ws: device workspace of at least mcs_anchor_workspace(p) bytes; a smaller
+ * one (but at least one head's group masses, G*N*4 bytes, and the grouping
+ * workspace) processes fewer heads per selection pass.
+ */
+mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, const void* v,
+                             int32_t* perm, int32_t* idx, void* dense_out, float* lse,
+                             void* residual, float* retained, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MCS_H_ */

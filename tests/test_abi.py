@@ -1,0 +1,88 @@
+"""Host-side checks of the C ABI (CPU only: no kernel runs here).
+
+The library must build, load, export every function include/mcs.h declares,
+and reject bad arguments on the host before any launch.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from token_sparse_attention_gb300 import build as mcs_build
+from token_sparse_attention_gb300 import mcs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    mcs_build.build()
+    return mcs.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mcs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mcs_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_binding_names():
+    assert declared_functions() == sorted(mcs.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    nm = os.popen(f"nm -D --defined-only {mcs.library_path()}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", nm), name
+
+
+def test_status_strings(L):
+    for code, name in mcs.STATUS_NAMES.items():
+        assert mcs.mcs_status_string(code) == name
+
+
+def test_host_validation_rejects_bad_arguments(L):
+    null = None
+    # null params
+    assert L.mcs_dense_attn(None, null, null, null, null, null, null) == 1
+    # unsupported head dim / group size
+    p = mcs.params(1, 2, 256, 96, 64, 40)
+    assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 16, 16, None, None) == 2
+    p = mcs.params(1, 2, 256, 128, 32, 40)
+    assert L.mcs_sparse_attn(ctypes.byref(p), 16, 16, 16, 16, 16, None, 16, None) == 2
+    # K out of range
+    p = mcs.params(1, 2, 256, 128, 64, 0)
+    assert L.mcs_sparse_attn(ctypes.byref(p), 16, 16, 16, 16, 16, None, 16, None) == 1
+    p = mcs.params(1, 2, 256, 128, 64, 257)
+    assert L.mcs_sparse_attn(ctypes.byref(p), 16, 16, 16, 16, 16, None, 16, None) == 1
+    # null tensor pointer
+    p = mcs.params(1, 2, 256, 128, 64, 40)
+    assert L.mcs_sparse_attn(ctypes.byref(p), 16, 16, None, 16, 16, None, 16, None) == 1
+    # misaligned bf16 pointer
+    assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 24, 16, None, None) == 1
+    # too many heads for the grid
+    p = mcs.params(2, 40000, 64, 128, 64, 10)
+    assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 16, 16, None, None) == 1
+    # negative scale
+    p = mcs.params(1, 1, 64, 128, 64, 10, scale=-1.0)
+    assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 16, 16, None, None) == 1
+    # workspace missing / too small
+    p = mcs.params(1, 2, 2048, 128, 64, 410)
+    assert L.mcs_group(ctypes.byref(p), 16, 16, None, 0, None) == 3
+    assert L.mcs_anchor_select(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, None, 16, 64,
+                               None) == 3
+
+
+def test_workspace_queries(L):
+    p = mcs.params(1, 2, 2048, 128, 64, 410)
+    g = mcs.mcs_group_workspace(p)
+    a = mcs.mcs_anchor_workspace(p)
+    assert g > 0 and a >= g
+    # at least one head of group masses (G x N fp32)
+    assert a >= p.G * p.N * 4
+    bad = mcs.params(1, 2, 2048, 96, 64, 410)
+    assert mcs.mcs_group_workspace(bad) == 0

@@ -1,0 +1,326 @@
+"""GPU parity of each library entry point against the fp64 oracle, on sizes
+the oracle finishes in seconds that still span several tiles and a ragged
+tail, plus edge cases.  Every call goes through the C ABI (libmcs.so)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mcs_oracle as orc
+from tests import parity as P
+from token_sparse_attention_gb300 import build as mcs_build
+from token_sparse_attention_gb300 import mcs
+from token_sparse_attention_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mcs_build.build()
+    mcs.lib()
+    assert torch.cuda.is_available()
+    yield
+    assert mcs.mcs_device_status() == 0
+
+
+def _dev(*ts):
+    return [t.cuda().contiguous() for t in ts]
+
+
+def _i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+# ---------------------------------------------------------------- dense + LSE
+
+@pytest.mark.parametrize("B,H,N,D", [(1, 1, 1, 128), (1, 1, 128, 128), (2, 2, 300, 128),
+                                     (1, 2, 517, 64), (1, 1, 129, 64), (1, 2, 1000, 128)])
+def test_dense_attention(B, H, N, D):
+    q, k, v = P.random_qkv(B, H, N, D, seed=N + D)
+    qd, kd, vd = _dev(q, k, v)
+    out = torch.empty_like(qd)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    p = mcs.params(B, H, N, D, 128, N)
+    mcs.mcs_dense_attn(p, qd, kd, vd, out, lse)
+    torch.cuda.synchronize()
+    scale = orc.default_scale(D)
+    for b in range(B):
+        for h in range(H):
+            O, L = orc.dense_attention(P.f64(q[b, h]), P.f64(k[b, h]), P.f64(v[b, h]), scale)
+            P.assert_close(out[b, h], O, f"dense out b{b} h{h}")
+            assert np.max(np.abs(P.f64(lse[b, h]) - L)) <= P.LSE_ABS
+
+
+def test_dense_attention_workload_tiny():
+    w = synth.workload("tiny")
+    q, k, v = synth.make_qkv(w, 0)
+    qd, kd, vd = _dev(q, k, v)
+    out = torch.empty_like(qd)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
+    mcs.mcs_dense_attn(p, qd, kd, vd, out, lse)
+    scale = orc.default_scale(w.D)
+    for h in range(w.H):
+        O, L = orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale)
+        P.assert_close(out[0, h], O, f"dense h{h}")
+        assert np.max(np.abs(P.f64(lse[0, h]) - L)) <= P.LSE_ABS
+
+
+# ---------------------------------------------------------------- sparse
+
+def _sparse_case(B, H, N, D, C, K, seed):
+    q, k, v = P.random_qkv(B, H, N, D, seed)
+    G = -(-N // C)
+    perm = np.stack([np.stack([P.random_groups(N, C, seed * 31 + b * H + h) for h in range(H)])
+                     for b in range(B)])
+    idx = np.stack([np.stack([P.random_idx(N, G, K, seed * 17 + b * H + h) for h in range(H)])
+                    for b in range(B)])
+    return q, k, v, perm, idx
+
+
+@pytest.mark.parametrize("B,H,N,D,C,K", [(1, 2, 512, 128, 128, 200), (2, 1, 300, 128, 128, 129),
+                                         (1, 2, 517, 128, 64, 77), (1, 1, 640, 64, 64, 128),
+                                         (1, 2, 333, 64, 128, 333), (1, 1, 200, 128, 64, 1)])
+def test_sparse_attention(B, H, N, D, C, K):
+    q, k, v, perm, idx = _sparse_case(B, H, N, D, C, K, seed=N + K)
+    qd, kd, vd = _dev(q, k, v)
+    out = torch.full_like(qd, float("nan"))
+    p = mcs.params(B, H, N, D, C, K)
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), None, out)
+    scale = orc.default_scale(D)
+    for b in range(B):
+        for h in range(H):
+            want = orc.sparse_attention(P.f64(q[b, h]), P.f64(k[b, h]), P.f64(v[b, h]),
+                                        perm[b, h], idx[b, h], C, scale)
+            P.assert_close(out[b, h], want, f"sparse b{b} h{h}")
+
+
+def test_sparse_residual_add_and_record():
+    B, H, N, D, C, K = 1, 2, 700, 128, 128, 150
+    q, k, v, perm, idx = _sparse_case(B, H, N, D, C, K, seed=5)
+    g = torch.Generator().manual_seed(6)
+    res = (0.1 * torch.randn(B, H, N, D, generator=g)).to(torch.bfloat16)
+    dense_in = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16)
+    qd, kd, vd, rd, dd = _dev(q, k, v, res, dense_in)
+    p = mcs.params(B, H, N, D, C, K)
+    out = torch.empty_like(qd)
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), rd, out)
+    rec = torch.empty_like(qd)
+    mcs.mcs_sparse_attn_record(p, qd, kd, vd, _i32(perm), _i32(idx), dd, rec)
+    scale = orc.default_scale(D)
+    for h in range(H):
+        sp = orc.sparse_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), perm[0, h],
+                                  idx[0, h], C, scale)
+        P.assert_close(out[0, h], sp + P.f64(res[0, h]), "reuse output")
+        # recorded residual relative to the magnitude of the output it corrects
+        ma, _ = P.err(rec[0, h], P.f64(dense_in[0, h]) - sp)
+        assert ma <= P.MAX_ABS
+        assert np.abs(P.f64(rec[0, h]) - (P.f64(dense_in[0, h]) - sp)).sum() <= \
+            P.MEAN_REL * np.abs(P.f64(dense_in[0, h])).sum()
+
+
+def test_sparse_full_density_equals_dense():
+    B, H, N, D, C = 1, 2, 384, 128, 128
+    q, k, v = P.random_qkv(B, H, N, D, 9)
+    qd, kd, vd = _dev(q, k, v)
+    G = -(-N // C)
+    perm = np.stack([P.random_groups(N, C, 10 + h) for h in range(H)])[None]
+    idx = np.tile(np.arange(N), (B, H, G, 1))
+    p = mcs.params(B, H, N, D, C, N)
+    sp = torch.empty_like(qd)
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), None, sp)
+    de = torch.empty_like(qd)
+    mcs.mcs_dense_attn(p, qd, kd, vd, de, None)
+    P.assert_close(sp, P.f64(de), "s=1 sparse vs dense", max_abs=2 ** -7, mean_rel=1e-3)
+
+
+def test_sparse_bad_index_reports_bounds():
+    B, H, N, D, C, K = 1, 1, 256, 128, 128, 64
+    q, k, v, perm, idx = _sparse_case(B, H, N, D, C, K, seed=3)
+    idx[0, 0, 1, 5] = N + 7  # out of range: clamped on the device and reported
+    qd, kd, vd = _dev(q, k, v)
+    out = torch.empty_like(qd)
+    p = mcs.params(B, H, N, D, C, K)
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), None, out)
+    assert mcs.mcs_device_status() == 6
+    assert mcs.mcs_device_status() == 0
+
+
+# ---------------------------------------------------------------- group mass + top-K
+
+@pytest.mark.parametrize("N,D,C", [(600, 128, 128), (517, 64, 64), (1024, 128, 64)])
+def test_group_mass_and_topk(N, D, C):
+    B, H = 1, 2
+    K = max(1, round(0.2 * N))
+    q, k, v = P.random_qkv(B, H, N, D, seed=N * 3 + D)
+    scale = orc.default_scale(D)
+    perm = np.stack([P.random_groups(N, C, 40 + h) for h in range(H)])[None]
+    lse = np.stack([orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale)[1]
+                    for h in range(H)])[None]
+    G = -(-N // C)
+    qd, kd = _dev(q, k)
+    lse_d = torch.from_numpy(lse.astype(np.float32)).cuda()
+    p = mcs.params(B, H, N, D, C, K)
+    mass = torch.empty(H, G, N, dtype=torch.float32, device="cuda")
+    mcs.mcs_group_mass(p, qd, kd, lse_d, _i32(perm), 0, H, mass)
+    idx = torch.empty(H * G, K, dtype=torch.int32, device="cuda")
+    ret = torch.empty(H * G, dtype=torch.float32, device="cuda")
+    mcs.mcs_topk(p, mass, idx, ret)
+    mass_h, idx_h, ret_h = P.f64(mass), idx.cpu().numpy(), P.f64(ret)
+    lse32 = lse.astype(np.float32).astype(np.float64)
+    oracle_masses = []
+    for h in range(H):
+        for g in range(G):
+            members = orc.group_members(perm[0, h], g, C)
+            want = orc.group_mass(P.f64(q[0, h]), P.f64(k[0, h]), lse32[0, h], members, scale)
+            got = mass_h[h, g]
+            assert np.all(np.abs(got - want) <= P.MASS_REL * want + 1e-12 * len(members)), \
+                f"mass h{h} g{g}: worst rel {np.max(np.abs(got - want) / np.maximum(want, 1e-30)):.3g}"
+            # selection from the GPU's masses against the oracle's: equal up to ties
+            row = h * G + g
+            sel, kept = orc.topk_select(want, K)
+            P.assert_topk_within_ties(idx_h[row], sel, want, K)
+            assert abs(ret_h[row] - kept) <= 1e-4 * kept
+            oracle_masses.append(want)
+    # top-K alone, on the oracle's masses rounded to fp32: the decision is taken
+    # in the same precision on both sides, so the index sets must be identical
+    m32 = np.stack(oracle_masses).astype(np.float32)
+    idx2 = torch.empty(m32.shape[0], K, dtype=torch.int32, device="cuda")
+    ret2 = torch.empty(m32.shape[0], dtype=torch.float32, device="cuda")
+    mcs.mcs_topk(p, torch.from_numpy(m32).cuda(), idx2, ret2)
+    got2 = idx2.cpu().numpy()
+    for r in range(m32.shape[0]):
+        sel, kept = orc.topk_select(m32[r].astype(np.float64), K)
+        assert np.array_equal(got2[r], sel), f"top-K on identical fp32 masses, row {r}"
+        assert abs(float(ret2[r]) - kept) <= 1e-5 * kept
+
+
+@pytest.mark.parametrize("rows,n,K", [(3, 1000, 1), (5, 4097, 777), (2, 300, 300), (4, 70000, 14000)])
+def test_topk_ties_and_shapes(rows, n, K):
+    rng = np.random.default_rng(n + K)
+    # few distinct values -> many exact ties; zeros included
+    mass = rng.integers(0, 7, size=(rows, n)).astype(np.float32) * 0.125
+    p = mcs.params(1, 1, n, 128, 128, K)
+    md = torch.from_numpy(mass).cuda()
+    idx = torch.empty(rows, K, dtype=torch.int32, device="cuda")
+    ret = torch.empty(rows, dtype=torch.float32, device="cuda")
+    mcs.mcs_topk(p, md, idx, ret)
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        sel, kept = orc.topk_select(mass[r].astype(np.float64), K)
+        assert np.array_equal(got[r], sel)
+        assert abs(float(ret[r]) - kept) <= 1e-6 * max(kept, 1.0)
+
+
+# ---------------------------------------------------------------- PDDP
+
+@pytest.mark.parametrize("N,C,D", [(2048, 64, 128), (3000, 128, 128), (1000, 64, 64), (4096, 128, 64)])
+def test_pddp_recovers_clusters(N, C, D):
+    x, want = P.separated_clusters(N, C, D, seed=N + C + D)
+    np.testing.assert_array_equal(orc.pddp_perm(x, C, 32), want)  # the oracle agrees
+    q = P.bf16_tensor(x)[None, None]
+    p = mcs.params(1, 1, N, D, C, 1)
+    perm = torch.empty(1, 1, p.G * C, dtype=torch.int32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_group_workspace(p))
+    mcs.mcs_group(p, q, perm, ws)
+    np.testing.assert_array_equal(perm[0, 0].cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name", ["tiny"])
+def test_pddp_valid_and_close_to_oracle(name):
+    w = synth.workload(name)
+    q, _, _ = synth.make_qkv(w, 0)
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
+    perm = torch.empty(w.B, w.H, p.G * w.C, dtype=torch.int32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_group_workspace(p))
+    mcs.mcs_group(p, q.cuda(), perm, ws)
+    got = perm.cpu().numpy()
+    for h in range(w.H):
+        P.check_valid_perm(got[0, h], w.N, w.C)
+        want = orc.pddp_perm(P.f64(q[0, h]), w.C, 32)
+        # fraction of tokens placed in the same group as the oracle (fp32 vs fp64
+        # projections may swap near-median tokens)
+        gid_got = np.empty(w.N, int)
+        gid_want = np.empty(w.N, int)
+        for g in range(p.G):
+            gid_got[orc.group_members(got[0, h], g, w.C)] = g
+            gid_want[orc.group_members(want, g, w.C)] = g
+        assert np.mean(gid_got == gid_want) >= 0.95
+
+
+def test_pddp_ragged_and_degenerate():
+    # N not a multiple of C, and a head whose queries are all identical (any
+    # split is a valid median split there: only validity is checked)
+    N, C, D = 1000, 128, 128
+    q, _, _ = P.random_qkv(1, 2, N, D, seed=77)
+    q[0, 1] = q[0, 1, 0]
+    p = mcs.params(1, 2, N, D, C, 1)
+    perm = torch.empty(1, 2, p.G * C, dtype=torch.int32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_group_workspace(p))
+    mcs.mcs_group(p, q.cuda(), perm, ws)
+    for h in range(2):
+        P.check_valid_perm(perm[0, h].cpu().numpy(), N, C)
+
+
+# ---------------------------------------------------------------- anchor step
+
+def test_anchor_select_on_clusters_matches_oracle():
+    N, C, D, H = 1024, 64, 128, 2
+    K = 200
+    xs = [P.separated_clusters(N, C, D, seed=100 + h) for h in range(H)]
+    q = torch.stack([torch.from_numpy(x).float() for x, _ in xs])[None].to(torch.bfloat16)
+    g = torch.Generator().manual_seed(5)
+    k = (q.float() + 0.5 * torch.randn(q.shape, generator=g)).to(torch.bfloat16)
+    v = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    p = mcs.params(1, H, N, D, C, K)
+    qd, kd, vd = _dev(q, k, v)
+    perm = torch.empty(1, H, p.G * C, dtype=torch.int32, device="cuda")
+    idx = torch.empty(1, H, p.G, K, dtype=torch.int32, device="cuda")
+    dense = torch.empty_like(qd)
+    res = torch.empty_like(qd)
+    lse = torch.empty(1, H, N, dtype=torch.float32, device="cuda")
+    ret = torch.empty(1, H, p.G, dtype=torch.float32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+    mcs.mcs_anchor_select(p, qd, kd, vd, perm, idx, dense, lse, res, ws, retained=ret)
+    scale = orc.default_scale(D)
+    for h in range(H):
+        a = orc.anchor_step(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), C, K, scale)
+        np.testing.assert_array_equal(perm[0, h].cpu().numpy(), a["perm"])
+        P.assert_close(dense[0, h], a["dense"], "anchor dense")
+        gi = idx[0, h].cpu().numpy()
+        for gg in range(p.G):
+            P.assert_topk_within_ties(gi[gg], a["idx"][gg], a["mass"][gg], K)
+        np.testing.assert_allclose(P.f64(ret[0, h]), a["retained"], rtol=1e-4)
+        # residual: R + O' reproduces the stored dense output
+        r = P.f64(res[0, h])
+        assert np.max(np.abs(r + a["sparse"] - P.f64(dense[0, h]))) <= P.MAX_ABS
+
+
+def test_anchor_then_reuse_identities_tiny_workload():
+    w = synth.workload("tiny")
+    K = w.K(0.2)
+    q, k, v = _dev(*synth.make_qkv(w, 0))
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
+    perm = torch.empty(1, w.H, p.G * w.C, dtype=torch.int32, device="cuda")
+    idx = torch.empty(1, w.H, p.G, K, dtype=torch.int32, device="cuda")
+    dense = torch.empty_like(q)
+    res = torch.empty_like(q)
+    lse = torch.empty(1, w.H, w.N, dtype=torch.float32, device="cuda")
+    ret = torch.empty(1, w.H, p.G, dtype=torch.float32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+    mcs.mcs_anchor_select(p, q, k, v, perm, idx, dense, lse, res, ws, retained=ret)
+    # reuse with the anchor's own inputs gives the dense output back
+    out = torch.empty_like(q)
+    mcs.mcs_sparse_attn(p, q, k, v, perm, idx, res, out)
+    P.assert_close(out, P.f64(dense), "reuse(same inputs) vs dense", max_abs=2 ** -6)
+    gi = idx.cpu().numpy()
+    assert np.all(np.diff(gi, axis=-1) > 0) and gi.min() >= 0 and gi.max() < w.N
+    sizes = np.array([min(w.C, w.N - g * w.C) for g in range(p.G)])
+    assert np.all(P.f64(ret) <= sizes * (1 + 1e-5))
+    # the dense output against the oracle
+    scale = orc.default_scale(w.D)
+    for h in range(w.H):
+        P.check_valid_perm(perm[0, h].cpu().numpy(), w.N, w.C)
+        O, _ = orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale)
+        P.assert_close(dense[0, h], O, "anchor dense (tiny)")

@@ -1,0 +1,69 @@
+// Internal launcher declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mcs {
+
+// Device status bits, OR-ed into the library's status word.
+enum : unsigned {
+  DEV_TIMEOUT = 1u,  // a bounded wait gave up
+  DEV_BOUNDS = 2u,   // an index read from an argument was out of range
+};
+
+// Attention kernel modes.
+enum AttnMode : int {
+  kDense = 0,         // dense attention, writes O (+ LSE)
+  kSparse = 1,        // token-sparse attention, writes O' scattered to perm rows
+  kSparseAdd = 2,     // token-sparse attention + cached residual (reuse step)
+  kSparseRecord = 3,  // token-sparse attention, writes residual = dense_out - O' (anchor)
+};
+
+struct AttnArgs {
+  int N;             // tokens per head
+  int C;             // queries per group (sparse modes)
+  int G;             // groups per head (sparse modes)
+  int K;             // selected KV tokens per group (sparse modes)
+  float scale_log2;  // softmax scale * log2(e)
+  __nv_bfloat16* out;            // [BH, N, D]; kSparseRecord: residual out
+  float* lse;                    // [BH, N] natural-log LSE (kDense, nullable)
+  const int32_t* perm;           // [BH, G*C]
+  const int32_t* idx;            // [BH, G, K]
+  const __nv_bfloat16* aux_in;   // kSparseAdd: residual; kSparseRecord: dense_out
+  unsigned* status;              // device status word
+};
+
+// tq/tk/tv: dense -> 3-D tile maps [BH][N][D], box {64,128,1};
+//           sparse -> 2-D gather maps [BH*N][D], box {64,1}.
+cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUtensorMap* tk,
+                             const CUtensorMap* tv, const AttnArgs& a, int BH,
+                             cudaStream_t stream);
+
+struct MassArgs {
+  int N, C, G;
+  int head0;              // first (b*H+h) head of this chunk
+  float scale_log2;
+  const int32_t* perm;    // [BH, G*C]
+  const float* lse;       // [BH, N]
+  float* mass;            // [heads in chunk, G, N]
+  unsigned* status;
+};
+
+// tq: 2-D gather map over Q [BH*N][D]; tk: 3-D tile map over K.
+cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const MassArgs& a, int heads, cudaStream_t stream);
+
+// rows x n masses -> rows x K ascending indices (+ retained sums, nullable).
+cudaError_t launch_topk(const float* mass, int rows, int n, int K, int32_t* idx, float* retained,
+                        unsigned* status, cudaStream_t stream);
+
+size_t pddp_workspace_bytes(int BH, int N, int D, int C);
+cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int BH, int N, int D,
+                        int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,
+                        unsigned* status, cudaStream_t stream);
+
+}  // namespace mcs

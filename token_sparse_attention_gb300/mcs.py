@@ -1,0 +1,234 @@
+"""Thin Python binding of libmcs.so (the C ABI declared in include/mcs.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on a CUDA device, checks dtype/shape/contiguity, and passes raw device
+pointers and the current CUDA stream to the C entry point of the same name.
+Every step of the computation runs in the library's kernels; there is no
+fallback of any kind.  If libmcs.so is missing or fails to load, the first
+call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "McsError", "Params", "params", "lib", "library_path", "EXPORTED",
+    "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status",
+    "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
+    "mcs_group_mass", "mcs_topk", "mcs_sparse_attn", "mcs_sparse_attn_record",
+    "mcs_anchor_select",
+]
+
+# Every symbol include/mcs.h declares.
+EXPORTED = (
+    "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
+    "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
+    "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select",
+)
+
+STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
+                3: "MCS_ERR_WORKSPACE", 4: "MCS_ERR_CUDA", 5: "MCS_ERR_TIMEOUT",
+                6: "MCS_ERR_BOUNDS"}
+
+
+class McsError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+class Params(ctypes.Structure):
+    """mcs_params: B, H, N, D, C, K, scale (0 -> 1/sqrt(D)), pddp_iters (0 -> 32)."""
+
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("D", ctypes.c_int), ("C", ctypes.c_int), ("K", ctypes.c_int),
+                ("scale", ctypes.c_float), ("pddp_iters", ctypes.c_int)]
+
+    @property
+    def G(self) -> int:
+        return -(-self.N // self.C)
+
+
+def params(B, H, N, D, C=128, K=None, scale=0.0, pddp_iters=0) -> Params:
+    return Params(B, H, N, D, C, N if K is None else K, scale, pddp_iters)
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmcs.so")
+
+
+_LIB = None
+_vp, _sz, _i, _st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int
+_pp = ctypes.POINTER(Params)
+
+_SIGS = {
+    "mcs_status_string": ([_st], ctypes.c_char_p),
+    "mcs_last_cuda_error": ([], ctypes.c_char_p),
+    "mcs_device_status": ([_vp], _st),
+    "mcs_group_workspace": ([_pp], _sz),
+    "mcs_anchor_workspace": ([_pp], _sz),
+    "mcs_group": ([_pp, _vp, _vp, _vp, _sz, _vp], _st),
+    "mcs_dense_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
+    "mcs_group_mass": ([_pp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp], _st),
+    "mcs_topk": ([_pp, _vp, _i, _vp, _vp, _vp], _st),
+    "mcs_sparse_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
+    "mcs_sparse_attn_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
+    "mcs_anchor_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmcs.so (built in-tree by build.py).  Raises if absent."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built; run __graft_entry__.build() first")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _LIB = L
+    return _LIB
+
+
+# ---------------------------------------------------------------- helpers
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t, dtype, shape=None, name="tensor", optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = lib().mcs_last_cuda_error().decode() if status == 4 else ""
+        raise McsError(status, where, detail)
+
+
+def _qkv_shape(p: Params):
+    return (p.B, p.H, p.N, p.D)
+
+
+# ---------------------------------------------------------------- entry points
+
+def mcs_status_string(status: int) -> str:
+    return lib().mcs_status_string(status).decode()
+
+
+def mcs_last_cuda_error() -> str:
+    return lib().mcs_last_cuda_error().decode()
+
+
+def mcs_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib().mcs_device_status(_stream(stream))
+
+
+def mcs_group_workspace(p: Params) -> int:
+    return lib().mcs_group_workspace(ctypes.byref(p))
+
+
+def mcs_anchor_workspace(p: Params) -> int:
+    return lib().mcs_anchor_workspace(ctypes.byref(p))
+
+
+def mcs_group(p: Params, q, perm, ws, stream=None):
+    bf = torch.bfloat16
+    _check(lib().mcs_group(ctypes.byref(p), _ptr(q, bf, _qkv_shape(p), "q"),
+                           _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+                           _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)),
+           "mcs_group")
+
+
+def mcs_dense_attn(p: Params, q, k, v, out, lse=None, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_dense_attn(ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
+                                _ptr(v, bf, s, "v"), _ptr(out, bf, s, "out"),
+                                _ptr(lse, torch.float32, s[:3], "lse", optional=True),
+                                _stream(stream)), "mcs_dense_attn")
+
+
+def mcs_group_mass(p: Params, q, k, lse, perm, head_begin, head_count, mass, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_group_mass(ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
+                                _ptr(lse, torch.float32, s[:3], "lse"),
+                                _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+                                int(head_begin), int(head_count),
+                                _ptr(mass, torch.float32, (head_count, p.G, p.N), "mass"),
+                                _stream(stream)), "mcs_group_mass")
+
+
+def mcs_topk(p: Params, mass, idx, retained=None, stream=None):
+    rows = mass.numel() // p.N
+    _check(lib().mcs_topk(ctypes.byref(p), _ptr(mass, torch.float32, None, "mass"), rows,
+                          _ptr(idx, torch.int32, None, "idx"),
+                          _ptr(retained, torch.float32, None, "retained", optional=True),
+                          _stream(stream)), "mcs_topk")
+    if idx.numel() != rows * p.K:
+        raise ValueError("idx must hold rows * K entries")
+
+
+def mcs_sparse_attn(p: Params, q, k, v, perm, idx, residual, out, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_sparse_attn(ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
+                                 _ptr(v, bf, s, "v"),
+                                 _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+                                 _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+                                 _ptr(residual, bf, s, "residual", optional=True),
+                                 _ptr(out, bf, s, "out"), _stream(stream)), "mcs_sparse_attn")
+
+
+def mcs_sparse_attn_record(p: Params, q, k, v, perm, idx, dense_out, residual, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_sparse_attn_record(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"), _ptr(v, bf, s, "v"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(dense_out, bf, s, "dense_out"), _ptr(residual, bf, s, "residual"),
+        _stream(stream)), "mcs_sparse_attn_record")
+
+
+def mcs_anchor_select(p: Params, q, k, v, perm, idx, dense_out, lse, residual, ws,
+                      retained=None, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_anchor_select(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"), _ptr(v, bf, s, "v"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(dense_out, bf, s, "dense_out"), _ptr(lse, torch.float32, s[:3], "lse"),
+        _ptr(residual, bf, s, "residual"),
+        _ptr(retained, torch.float32, (p.B, p.H, p.G), "retained", optional=True),
+        _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)), "mcs_anchor_select")
+
+
+def empty_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A device byte buffer of at least nbytes (256-byte aligned by torch)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)
