@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = threadIdx.x;  // 0..127 == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       if (!warp_wait(s_full, j & 1, abort_flag, a.status)) { ok = false; break; }
@@ -251,11 +251,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
       const float m_new = mx * sl2;
-      if (j == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + kRescaleThreshold) {
-        const float f = ex2(m_run - m_new);
-        l_run *= f;
+      // Lazy rescaling: a row's reference max only moves when the tile max
+      // exceeds it by more than the threshold.  TMEM loads/stores are
+      // warp-collective, so the whole warp enters the rescale when any of its
+      // rows needs it (f = 1 for the others).
+      const bool need = (j > 0) && (m_new > m_run + kRescaleThreshold);
+      if (j == 0) m_run = m_new;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? ex2(m_run - m_new) : 1.f;
+        l_f32 *= f;
+        l_b16 *= f;
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
           uint32_t o[16];
@@ -265,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(f * __uint_as_float(o[i]));
           tmem_st16(tO + lane_off + c * 16, o);
         }
-        m_run = m_new;
+        if (need) m_run = m_new;
       }
-      float sum = 0.f;
+      float sum_f = 0.f, sum_b = 0.f;
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
@@ -275,12 +280,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, -m_run));
           const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, -m_run));
-          sum += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
+          sum_f += p0 + p1;
+          // the output is normalised by the sum of the bf16 weights the PV
+          // product actually uses; the LSE by the fp32 sum
+          sum_b += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
         }
         tmem_st16(tS + lane_off + c * 16, pk);
       }
-      l_run += sum;
+      l_f32 += sum_f;
+      l_b16 += sum_b;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------------------------------------ epilogue
     if (ok && warp_wait(o_full, 0, abort_flag, a.status)) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = 1.f / l_b16;
       int token;
       if (MODE == kDense) {
         token = tile * BM + row;
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (MODE == kDense && a.lse != nullptr && token >= 0)
-        a.lse[static_cast<size_t>(bh) * a.N + token] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        a.lse[static_cast<size_t>(bh) * a.N + token] = (m_run + __log2f(l_f32)) * 0.69314718055994531f;
     }
   }
 

@@ -39,7 +39,7 @@ import math
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_qkv", "positions"]
+__all__ = ["Workload", "WORKLOADS", "workload", "make_qkv", "make_qkv_like", "positions"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -179,3 +179,26 @@ def make_qkv(w: Workload, step: int = 0, heads=None, device="cpu",
             out[x][slot] = t.to(dtype)
     B = w.B if len(heads) == BH else 1
     return tuple(o.reshape(B, -1, w.N, w.D) for o in out)
+
+
+def make_qkv_like(B: int, H: int, N: int, D: int, seed: int, alpha: float = 2.7,
+                  device="cpu", dtype=torch.bfloat16):
+    """Q, K, V [B, H, N, D] for an arbitrary token count, built like the
+    workloads above (Fourier features of positions, per-head projections,
+    N(0, 0.3^2) noise, Q and K standardised, Q scaled by alpha) but with the
+    N positions drawn uniformly in the unit cube.  For small parity cases."""
+    g = _gen(seed, device)
+    pos = torch.rand(N, 3, generator=g, device=device)
+    omega = 4.0 * torch.randn(16, 3, generator=g, device=device)
+    ang = 2 * math.pi * (pos @ omega.T)
+    phi = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1)
+    out = []
+    for x in range(3):
+        proj = torch.randn(B * H, 32, D, generator=g, device=device) / math.sqrt(32.0)
+        t = phi[None] @ proj + 0.3 * torch.randn(B * H, N, D, generator=g, device=device)
+        if x < 2:
+            t = t / t.std(dim=(1, 2), keepdim=True)
+        if x == 0:
+            t = t * alpha
+        out.append(t.reshape(B, H, N, D).to(dtype))
+    return tuple(out)
