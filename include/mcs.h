@@ -97,9 +97,9 @@ mcs_status mcs_group(const mcs_params* p, const void* q, int32_t* perm, void* ws
                      cudaStream_t stream);
 
 /*
- * a2 -- Dense attention with per-query log-sum-exp, the selector's first
- * pass (ai.info AI summary, "Methodology in Plain English": "computes the
- * dense output and row-wise log-sum-exp values") and the speedup baseline.
+ * a2 -- Dense attention with per-query log-sum-exp: the selector's first
+ * pass, which yields both the dense output and every row's LSE (ai.info AI
+ * summary, "Methodology in Plain English"), and the speedup baseline.
  * out = softmax(scale * q k^T) v  [B,H,N,D] bf16;
  * lse = log sum_j exp(scale * q_i.k_j)  [B,H,N] fp32, nullable.
  */

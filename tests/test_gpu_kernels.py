@@ -330,3 +330,22 @@ def test_anchor_then_reuse_identities_tiny_workload():
         P.check_valid_perm(perm[0, h].cpu().numpy(), w.N, w.C)
         O, _ = orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale)
         P.assert_close(dense[0, h], O, "anchor dense (tiny)")
+
+
+def test_single_short_group():
+    # N < C: one group, no split; padding slots -1; sparse attention on it
+    N, D, C, K = 50, 128, 64, 20
+    q, k, v = P.random_qkv(1, 1, N, D, seed=50)
+    qd, kd, vd = _dev(q, k, v)
+    p = mcs.params(1, 1, N, D, C, K)
+    perm = torch.empty(1, 1, C, dtype=torch.int32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_group_workspace(p))
+    mcs.mcs_group(p, qd, perm, ws)
+    want = np.concatenate([np.arange(N), np.full(C - N, -1)])
+    np.testing.assert_array_equal(perm[0, 0].cpu().numpy(), want)
+    idx = P.random_idx(N, 1, K, 51)[None, None]
+    out = torch.empty_like(qd)
+    mcs.mcs_sparse_attn(p, qd, kd, vd, perm, _i32(idx), None, out)
+    sp = orc.sparse_attention(P.f64(q[0, 0]), P.f64(k[0, 0]), P.f64(v[0, 0]), want, idx[0, 0],
+                              C, orc.default_scale(D))
+    P.assert_close(out[0, 0], sp, "single short group")

@@ -1,0 +1,149 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times.
+
+The oracle cannot run whole heads of 75600 queries, so each workload is
+checked on sampled units the oracle computes one by one, plus properties that
+hold at any size:
+  * the whole anchor step on the GPU: valid groups for every head, selected
+    indices ascending and in range, retained mass at most the group size, and
+    reuse with the anchor's own inputs reproducing the dense output;
+  * dense attention and LSE on sampled query rows of two heads;
+  * group mass, top-K and sparse attention (+ residual) on sampled groups of
+    head 0, with the groups, LSE values and indices made by the oracle;
+  * agreement of the GPU grouping of head 0 with the oracle's.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mcs_oracle as orc
+from tests import parity as P
+from token_sparse_attention_gb300 import build as mcs_build
+from token_sparse_attention_gb300 import mcs
+from token_sparse_attention_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("small", 0.2), ("small", 0.1), ("large", 0.2), ("long", 0.15), ("asset3d", 0.15)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mcs_build.build()
+    mcs.lib()
+    assert torch.cuda.is_available()
+
+
+def _i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+@pytest.mark.parametrize("name,density", CASES)
+def test_workload_full_size(name, density):
+    w = synth.workload(name)
+    K = w.K(density)
+    BH = w.B * w.H
+    q, k, v = synth.make_qkv(w, 0, device="cuda")
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
+    G = p.G
+    perm = torch.empty(w.B, w.H, G * w.C, dtype=torch.int32, device="cuda")
+    idx = torch.empty(w.B, w.H, G, K, dtype=torch.int32, device="cuda")
+    dense = torch.empty_like(q)
+    res = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+    ret = torch.empty(w.B, w.H, G, dtype=torch.float32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+    mcs.mcs_anchor_select(p, q, k, v, perm, idx, dense, lse, res, ws, retained=ret)
+    assert mcs.mcs_device_status() == 0
+    del ws
+
+    # ---- properties of the whole anchor step
+    pm = perm.view(BH, -1).cpu().numpy()
+    for h in range(BH):
+        P.check_valid_perm(pm[h], w.N, w.C)
+    sizes = np.array([min(w.C, w.N - g * w.C) for g in range(G)])
+    assert np.all(P.f64(ret).reshape(BH, G) <= sizes * (1 + 1e-4))
+    for h in (0, BH - 1):
+        ih = idx.view(BH, G, K)[h].cpu().numpy()
+        assert ih.min() >= 0 and ih.max() < w.N and np.all(np.diff(ih, axis=1) > 0)
+    same = torch.empty_like(q)
+    mcs.mcs_sparse_attn(p, q, k, v, perm, idx, res, same)
+    d = (same.float() - dense.float()).abs()
+    assert d.max().item() <= 2 ** -5 and d.mean().item() <= 2e-3 * dense.float().abs().mean().item()
+
+    # ---- dense + LSE on sampled rows of two heads
+    scale = orc.default_scale(w.D)
+    rng = np.random.default_rng(7)
+    host = {}
+    for h in (0, BH - 1):
+        b, hh = divmod(h, w.H)
+        qh, kh, vh = (P.f64(t[b, hh]) for t in (q, k, v))
+        host[h] = (qh, kh, vh)
+        rows = np.sort(rng.choice(w.N, 64, replace=False))
+        O, L = orc.dense_attention(qh, kh, vh, scale, rows=rows)
+        P.assert_close(dense[b, hh][rows], O, f"{name} dense rows h{h}")
+        assert np.max(np.abs(P.f64(lse[b, hh][rows]) - L)) <= P.LSE_ABS
+
+    # ---- selection and sparse attention on oracle-made groups of head 0
+    qh, kh, vh = host[0]
+    operm = orc.pddp_perm(qh, w.C, 32)
+    groups = [0, G - 1] + list(rng.choice(np.arange(1, G - 1), 6, replace=False))
+    members = {g: orc.group_members(operm, g, w.C) for g in groups}
+    olse = np.zeros(w.N)
+    for g in groups:
+        olse[members[g]] = orc.dense_attention(qh, kh, vh, scale, rows=members[g])[1]
+    olse32 = olse.astype(np.float32)
+    perm_in = perm.clone()
+    perm_in.view(BH, -1)[0] = _i32(operm)
+    lse_in = lse.clone()
+    lse_in.view(BH, -1)[0] = torch.from_numpy(olse32).cuda()
+    mass = torch.empty(1, G, w.N, dtype=torch.float32, device="cuda")
+    mcs.mcs_group_mass(p, q, k, lse_in, perm_in, 0, 1, mass)
+    sel = torch.empty(G, K, dtype=torch.int32, device="cuda")
+    mcs.mcs_topk(p, mass, sel)
+    mass_h, sel_h = mass[0].cpu().numpy().astype(np.float64), sel.cpu().numpy()
+    oidx = idx.view(BH, G, K)[0].cpu().numpy().copy()  # any valid sets for other groups
+    for g in groups:
+        want = orc.group_mass(qh, kh, olse32.astype(np.float64), members[g], scale)
+        got = mass_h[g]
+        assert np.all(np.abs(got - want) <= P.MASS_REL * want + 1e-12 * len(members[g])), \
+            f"{name} mass g{g}"
+        o_sel = orc.topk_select(want, K)[0]
+        P.assert_topk_within_ties(sel_h[g], o_sel, want, K)
+        oidx[g] = o_sel
+    idx_in = idx.clone()
+    idx_in.view(BH, G, K)[0] = _i32(oidx)
+    g_res = torch.Generator().manual_seed(3)
+    r0 = (0.05 * torch.randn(w.N, w.D, generator=g_res, dtype=torch.float64)).to(torch.bfloat16)
+    res_in = res.clone()
+    res_in.view(BH, w.N, w.D)[0] = r0.cuda()
+    out = torch.empty_like(q)
+    mcs.mcs_sparse_attn(p, q, k, v, perm_in, idx_in, res_in, out)
+    out0 = out.view(BH, w.N, w.D)[0]
+    for g in groups:
+        m = members[g]
+        want = orc.sparse_attention_group(qh, kh, vh, m, oidx[g], scale) + P.f64(r0)[m]
+        P.assert_close(out0[torch.from_numpy(m).cuda()], want, f"{name} sparse g{g}")
+    assert mcs.mcs_device_status() == 0
+
+    # ---- grouping of head 0 against the oracle's (fp32 vs fp64 projections
+    # may move near-median tokens)
+    gid_got, gid_want = np.empty(w.N, int), np.empty(w.N, int)
+    for g in range(G):
+        gid_got[orc.group_members(pm[0], g, w.C)] = g
+        gid_want[orc.group_members(operm, g, w.C)] = g
+    agree = np.mean(gid_got == gid_want)
+    print(f"{name}: token groups agreeing with the oracle {agree:.4f}")
+    assert agree >= 0.9
+
+
+@pytest.mark.parametrize("N,C,D", [(75600, 128, 128), (65536, 64, 64)])
+def test_pddp_full_size_clusters(N, C, D):
+    x, want = P.separated_clusters(N, C, D, seed=N)
+    q = P.bf16_tensor(x)[None, None]
+    p = mcs.params(1, 1, N, D, C, 1)
+    perm = torch.empty(1, 1, p.G * C, dtype=torch.int32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_group_workspace(p))
+    mcs.mcs_group(p, q, perm, ws)
+    np.testing.assert_array_equal(perm[0, 0].cpu().numpy(), want)
