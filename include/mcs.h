@@ -166,6 +166,31 @@ mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, 
                              void* residual, float* retained, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/*
+ * Query grouping (as mcs_group) for callers that cannot allocate device
+ * memory.  No counterpart in the paper: this is a deployment variant.
+ *
+ * Some host programs cannot hand this library a workspace: a plugin inside
+ * another framework may be given only its input and output buffers, and
+ * servers that fix their memory footprint at start-up forbid any device
+ * allocation afterwards.  This entry point needs neither a workspace nor an
+ * allocation: its scratch is a 64 MiB array compiled into the library, which
+ * every GPU that loads this part of the library keeps until the process
+ * exits.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Same arguments and results as mcs_group, without ws/ws_bytes; heads are
+ * processed a batch at a time so that each batch fits the scratch.  Returns
+ * MCS_ERR_WORKSPACE, launching nothing, when a single head needs more than
+ * the 64 MiB (mcs_group_workspace for B = H = 1 exceeds 64 MiB).
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and nothing in it needs clearing between
+ * calls; calls that overlap on the GPU (two streams, or two host threads)
+ * race on it and must be serialised by the caller.
+ */
+mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int32_t* perm,
+                             cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

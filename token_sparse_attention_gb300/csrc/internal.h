@@ -61,6 +61,11 @@ cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* t
 cudaError_t launch_topk(const float* mass, int rows, int n, int K, int32_t* idx, float* retained,
                         unsigned* status, cudaStream_t stream);
 
+// Device address of the library's status word (for kernels' status argument).
+cudaError_t device_status_word(unsigned** out);
+// 2-D gather tensor map over `rows` bf16 rows of D columns (box {64, 1}).
+bool encode_gather_map(CUtensorMap* m, const void* base, long long rows, int D);
+
 size_t pddp_workspace_bytes(int BH, int N, int D, int C);
 cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int BH, int N, int D,
                         int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,

@@ -137,6 +137,15 @@ size_t mass_head_bytes(const mcs_params* p) {
 
 }  // namespace
 
+namespace mcs {
+cudaError_t device_status_word(unsigned** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_mcs_status);
+}
+bool encode_gather_map(CUtensorMap* m, const void* base, long long rows, int D) {
+  return make_gather_map(m, base, 1, static_cast<int>(rows), D);
+}
+}  // namespace mcs
+
 extern "C" {
 
 const char* mcs_status_string(mcs_status s) {

@@ -1,0 +1,79 @@
+// mcs_group_noalloc: query grouping for callers that cannot allocate device
+// memory.  Its scratch is a fixed array compiled into the library instead of
+// a caller-provided workspace; see the declaration in include/mcs.h.
+#include <mutex>
+
+#include "internal.h"
+#include "mcs.h"
+
+namespace {
+
+// Size of the built-in scratch.  Every GPU on which the library's grouping
+// module is loaded keeps this much device memory until the process exits.
+constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// In host code `g_noalloc_scratch` only names a host-side shadow of the
+// array; kernels must be given its device address, looked up once per device.
+constexpr int kMaxDevices = 256;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int32_t* perm,
+                                        cudaStream_t stream) {
+  if (p == nullptr || q == nullptr || perm == nullptr) return MCS_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 1 || (long long)p->B * p->H > 65535 ||
+      (long long)p->B * p->H * p->N > 0x7fffffffLL || p->pddp_iters < 0)
+    return MCS_ERR_INVALID_ARG;
+  if (p->D != 64 && p->D != 128) return MCS_ERR_UNSUPPORTED;
+  if (p->C != 64 && p->C != 128) return MCS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return MCS_ERR_INVALID_ARG;
+  const int BH = p->B * p->H, N = p->N, D = p->D, C = p->C;
+  const int G = (N + C - 1) / C;
+  const int iters = p->pddp_iters > 0 ? p->pddp_iters : 32;
+
+  // Heads are grouped a batch at a time through the fixed scratch.
+  const size_t one = mcs::pddp_workspace_bytes(1, N, D, C);
+  if (one > kNoallocScratchBytes) return MCS_ERR_WORKSPACE;  // too large for the built-in scratch
+  int batch = static_cast<int>(kNoallocScratchBytes / one);
+  if (batch > BH) batch = BH;
+  while (batch > 1 && mcs::pddp_workspace_bytes(batch, N, D, C) > kNoallocScratchBytes) --batch;
+
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return MCS_ERR_CUDA;
+  unsigned* status = nullptr;
+  if ((e = mcs::device_status_word(&status)) != cudaSuccess) return MCS_ERR_CUDA;
+
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
+  for (int h0 = 0; h0 < BH; h0 += batch) {
+    const int hc = BH - h0 < batch ? BH - h0 : batch;
+    const __nv_bfloat16* qh = qb + static_cast<size_t>(h0) * N * D;
+    CUtensorMap tq;
+    if (!mcs::encode_gather_map(&tq, qh, static_cast<long long>(hc) * N, D))
+      return MCS_ERR_CUDA;
+    e = mcs::launch_pddp(qh, &tq, hc, N, D, C, iters, perm + static_cast<size_t>(h0) * G * C,
+                         scratch, kNoallocScratchBytes, status, stream);
+    if (e != cudaSuccess) return MCS_ERR_CUDA;
+  }
+  return MCS_OK;
+}

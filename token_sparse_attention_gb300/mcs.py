@@ -21,14 +21,14 @@ __all__ = [
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status",
     "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
     "mcs_group_mass", "mcs_topk", "mcs_sparse_attn", "mcs_sparse_attn_record",
-    "mcs_anchor_select",
+    "mcs_anchor_select", "mcs_group_noalloc",
 ]
 
 # Every symbol include/mcs.h declares.
 EXPORTED = (
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
-    "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select",
+    "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
 )
 
 STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
@@ -80,6 +80,7 @@ _SIGS = {
     "mcs_sparse_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_sparse_attn_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_anchor_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
+    "mcs_group_noalloc": ([_pp, _vp, _vp, _vp], _st),
 }
 
 
@@ -162,6 +163,15 @@ def mcs_group(p: Params, q, perm, ws, stream=None):
                            _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
                            _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)),
            "mcs_group")
+
+
+def mcs_group_noalloc(p: Params, q, perm, stream=None):
+    """mcs_group for callers that cannot allocate: uses the library's built-in
+    64 MiB scratch instead of a workspace (see include/mcs.h)."""
+    bf = torch.bfloat16
+    _check(lib().mcs_group_noalloc(ctypes.byref(p), _ptr(q, bf, _qkv_shape(p), "q"),
+                                   _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+                                   _stream(stream)), "mcs_group_noalloc")
 
 
 def mcs_dense_attn(p: Params, q, k, v, out, lse=None, stream=None):
