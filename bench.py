@@ -24,6 +24,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mcs|reference
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -364,7 +365,7 @@ def run_gpu(args, w, K, rank, world, dist):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"large video B={w.B} H={w.H} N={w.N} (21x60x60) D={w.D} C={w.C} "
+            "workload": f"{w.name} B={w.B} H={w.H} N={w.N} D={w.D} C={w.C} "
                         f"density {args.density} K={K}",
             "step": "anchor (pddp, dense+lse, mass+top-k, sparse record) + reuse (sparse+residual)",
             "value_basis": "reuse-step sparse attention kernel time, CUDA events, mean of timed steps",
@@ -400,12 +401,16 @@ def main():
     ap.add_argument("--density", type=float, default=0.2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the head count (smaller cases for profiling; not a bench number)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = synth.workload(args.workload)
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
     K = w.K(args.density)
 
     if args.impl == "reference":

@@ -9,15 +9,22 @@
 // attention with row LSE is the selector's first pass (ai.info AI summary,
 // "Methodology in Plain English") and the speedup denominator.
 //
-// One CTA = one 128-row query tile (dense) or one query group (sparse) of one
-// head; two CTAs share an SM so that one's softmax overlaps the other's MMAs.
+// One CTA per SM; one CTA = one 128-row query tile (dense) or one query group
+// (sparse) of one head.
 //   warps 0-3  softmax + epilogue: thread t owns query row t = TMEM lane t
-//   warp 4     producer: TMA tile loads (dense) or TMA gather4 (sparse)
-//   warp 5     TMEM allocation and the single MMA-issuing thread
-// TMEM (256 columns): S = Q K^T in columns [0,128) (fp32), overwritten in
-// place by P (bf16 pairs) in columns [0,64); O accumulator in [128, 128+D).
-// Online softmax in base 2 with lazy rescaling (O is only rescaled when the
-// running max grows by more than 8, i.e. P stays <= 256).
+//   warps 4-10 producers: K and V tiles into a ring of kStages shared-memory
+//              stages, as far ahead as the ring allows.  Dense: one thread
+//              issues TMA tile loads.  Sparse: every K or V tile is 32*D/64
+//              TMA gather4 operations (4 rows x 64 columns each); they are
+//              spread over the 7 producer warps, one per lane, because the
+//              gather rate grows with the number of warps issuing them
+//   warp 11    TMEM allocation and the single MMA-issuing thread
+// TMEM (512 columns): two score buffers S0/S1 (128 fp32 columns each; P is
+// written over S as bf16 pairs) and the O accumulator.  The MMA order
+//   QK(0), QK(1), PV(0), QK(2), PV(1), QK(3), ...
+// lets the tensor core compute S(j+1) and PV(j-1) while the softmax warps
+// work on S(j).  Online softmax in base 2 with lazy rescaling (O is rescaled
+// only when a row's running max grows by more than 8, so P <= 256).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -26,22 +33,34 @@ namespace {
 
 constexpr int BM = 128;  // query rows per CTA (MMA M)
 constexpr int BN = 128;  // KV rows per tile (MMA N of QK^T, K of PV)
-constexpr int kThreads = 192;
+constexpr int kProducers = 7;
+constexpr int kMmaWarp = 4 + kProducers;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
 struct AttnLayout {
-  static constexpr int kSub = D / 64;             // 128-byte column sub-tiles per row
-  static constexpr int kSubBytes = 128 * 128;     // one sub-tile: 128 rows x 128 B
+  static constexpr int kSub = D / 64;          // 128-byte column sub-tiles per row
+  static constexpr int kSubBytes = 128 * 128;  // one sub-tile: 128 rows x 128 B
   static constexpr int kTileBytes = kSub * kSubBytes;
+  static constexpr int kStages = D == 128 ? 6 : 12;  // K/V ring depth (tiles)
   static constexpr int kQ = 0;
-  static constexpr int kK = kTileBytes;
-  static constexpr int kV = 2 * kTileBytes;
-  static constexpr int kBars = 3 * kTileBytes;
-  // At most two CTAs per SM: each holds 256 TMEM columns of the SM's 512.
-  static constexpr int kUsed = kBars + 128 + 1024;
-  static constexpr int kSmem = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
+  static constexpr int kRing = kTileBytes;
+  static constexpr int kBars = kRing + kStages * kTileBytes;
+  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
+
+// Sum of the eight fp32 partials held in four packed pairs.
+__device__ __forceinline__ float sum8(const uint64_t* acc) {
+  float a0, a1, a2, a3, a4, a5, a6, a7;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], a2, a3);
+  f2_unpack(acc[2], a4, a5);
+  f2_unpack(acc[3], a6, a7);
+  return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* status) {
@@ -58,26 +77,25 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
   using L = AttnLayout<D>;
+  constexpr int NS = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sq = smem + L::kQ;
-  uint8_t* sk = smem + L::kK;
-  uint8_t* sv = smem + L::kV;
+  uint8_t* ring = smem + L::kRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 2;
-  uint64_t* v_full = bars + 3;
-  uint64_t* v_empty = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_full = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* full = bars;              // [NS] stage loaded
+  uint64_t* empty = bars + NS;        // [NS] stage consumed by its MMA
+  uint64_t* q_full = bars + 2 * NS;
+  uint64_t* s_full = q_full + 1;      // [2] S(j) in buffer j&1 computed
+  uint64_t* p_full = q_full + 3;      // [2] P(j) written (4 warp arrivals)
+  uint64_t* o_done = q_full + 5;      // PV(j) complete
+  uint64_t* o_full = q_full + 6;      // every MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
@@ -88,140 +106,182 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int nkv = (kv_total + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, MODE == kDense ? 1 : kProducers);  // sparse: every producer warp
+      mbar_init(empty + s, 1);
+    }
     mbar_init(q_full, 1);
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    mbar_init(s_full + 0, 1);
+    mbar_init(s_full + 1, 1);
+    mbar_init(p_full + 0, 4);
+    mbar_init(p_full + 1, 4);
+    mbar_init(o_done, 1);
     mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + 128;
+  const uint32_t tO = tmem + 256;  // S0 at +0, S1 at +128
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int k_issued = 0, v_issued = 0;
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    // Ring item i = 2j (K tile j) or 2j+1 (V tile j) goes to stage i % NS.
+    int issued = 0;
     if (MODE == kDense) {
-      if (lane == 0) {
+      if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         mbar_expect_tx(q_full, L::kTileBytes);
         for (int s = 0; s < L::kSub; ++s)
           tma_load_3d(sq + s * L::kSubBytes, &tq, s * 64, tile * BM, bh, q_full);
-        for (int j = 0; j < nkv; ++j) {
-          if (j > 0 && !mbar_wait(k_empty, (j - 1) & 1, abort_flag, a.status)) break;
-          mbar_expect_tx(k_full, L::kTileBytes);
+        for (int i = 0; i < 2 * nkv; ++i) {
+          const int st = i % NS;
+          if (i >= NS && !mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
+          mbar_expect_tx(full + st, L::kTileBytes);
+          const CUtensorMap* tm = (i & 1) ? &tv : &tk;
+          uint8_t* dst = ring + st * L::kTileBytes;
           for (int s = 0; s < L::kSub; ++s)
-            tma_load_3d(sk + s * L::kSubBytes, &tk, s * 64, j * BN, bh, k_full);
-          ++k_issued;
-          if (j > 0 && !mbar_wait(v_empty, (j - 1) & 1, abort_flag, a.status)) break;
-          mbar_expect_tx(v_full, L::kTileBytes);
-          for (int s = 0; s < L::kSub; ++s)
-            tma_load_3d(sv + s * L::kSubBytes, &tv, s * 64, j * BN, bh, v_full);
-          ++v_issued;
+            tma_load_3d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, bh, full + st);
+          ++issued;
         }
         if (*abort_flag) {
-          if (k_issued) drain_wait(k_full, (k_issued - 1) & 1);
-          if (v_issued) drain_wait(v_full, (v_issued - 1) & 1);
+          for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+            drain_wait(full + (i % NS), (i / NS) & 1);
         }
       }
     } else {
-      // Sparse: Q rows by perm, K/V rows by idx, 4 rows per gather4; lane l
-      // fetches rows 4l..4l+3 of every tile.
+      // Sparse.  Gather operation q in [0, 32*kSub) of a tile (sub-tile
+      // q / 32, rows 4*(q % 32) .. +3) is issued by producer warp q % 7,
+      // lane q / 7.
       const size_t grp = static_cast<size_t>(bh) * a.G + tile;
       const int32_t* perm_g = a.perm + grp * a.C;
       const int32_t* idx_g = a.idx + grp * a.K;
       const int rowbase = bh * a.N;
-      int r[4];
+      const int pw = warp - 4;                       // 0..kProducers-1
+      const int q = pw + kProducers * lane;          // this lane's operation
+      const bool active = q < 32 * L::kSub;
+      const int nops = (32 * L::kSub - pw + kProducers - 1) / kProducers;  // this warp's count
+      const int sub = q / 32;
+      const int quad = q % 32;
       bool bad = false;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int p = 4 * lane + i;
-        int t = (p < a.C) ? __ldg(perm_g + p) : 0;
-        if (t < 0) t = 0;  // padding slot of the short last group
-        if (t >= a.N) { bad = true; t = 0; }
-        r[i] = rowbase + t;
-      }
-      if (lane == 0) {
-        tma_prefetch_desc(&tq);
-        tma_prefetch_desc(&tk);
-        tma_prefetch_desc(&tv);
-        mbar_expect_tx(q_full, L::kTileBytes);
-      }
-      __syncwarp();
-      for (int s = 0; s < L::kSub; ++s)
-        tma_gather4(sq + s * L::kSubBytes + lane * 4 * 128, &tq, s * 64, r[0], r[1], r[2], r[3],
-                    q_full);
-      for (int j = 0; j < nkv; ++j) {
+      int r[4];
+      if (warp == 4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          int c = j * BN + 4 * lane + i;
+          const int p = 4 * lane + i;
+          int t = (p < a.C) ? __ldg(perm_g + p) : 0;
+          if (t < 0) t = 0;  // padding slot of the short last group
+          if (t >= a.N) { bad = true; t = 0; }
+          r[i] = rowbase + t;
+        }
+        if (lane == 0) {
+          tma_prefetch_desc(&tq);
+          tma_prefetch_desc(&tk);
+          tma_prefetch_desc(&tv);
+          mbar_expect_tx(q_full, L::kTileBytes);
+        }
+        __syncwarp();
+        for (int s = 0; s < L::kSub; ++s)
+          tma_gather4(sq + s * L::kSubBytes + lane * 4 * 128, &tq, s * 64, r[0], r[1], r[2],
+                      r[3], q_full);
+      }
+      // Row indices of tile j are loaded two tiles ahead so their latency
+      // (the index array is read once, from HBM) stays off the critical path.
+      auto load_idx = [&](int j, int* out) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int c = j * BN + 4 * quad + i;
           c = c < a.K ? c : a.K - 1;  // tail columns repeat a valid row; masked in softmax
-          int t = __ldg(idx_g + c);
+          out[i] = active ? __ldg(idx_g + c) : 0;
+        }
+      };
+      int cur[4], nxt[4] = {0, 0, 0, 0};
+      load_idx(0, cur);
+      if (nkv > 1) load_idx(1, nxt);
+      bool stop = false;
+      for (int j = 0; j < nkv && !stop; ++j) {
+        int ahead[4] = {0, 0, 0, 0};
+        if (j + 2 < nkv) load_idx(j + 2, ahead);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int t = cur[i];
           if (t < 0 || t >= a.N) { bad = true; t = 0; }
           r[i] = rowbase + t;
         }
-        if (j > 0 && !warp_wait(k_empty, (j - 1) & 1, abort_flag, a.status)) break;
-        if (lane == 0) mbar_expect_tx(k_full, L::kTileBytes);
-        __syncwarp();
-        for (int s = 0; s < L::kSub; ++s)
-          tma_gather4(sk + s * L::kSubBytes + lane * 4 * 128, &tk, s * 64, r[0], r[1], r[2], r[3],
-                      k_full);
-        ++k_issued;
-        if (j > 0 && !warp_wait(v_empty, (j - 1) & 1, abort_flag, a.status)) break;
-        if (lane == 0) mbar_expect_tx(v_full, L::kTileBytes);
-        __syncwarp();
-        for (int s = 0; s < L::kSub; ++s)
-          tma_gather4(sv + s * L::kSubBytes + lane * 4 * 128, &tv, s * 64, r[0], r[1], r[2], r[3],
-                      v_full);
-        ++v_issued;
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * j + kv;
+          const int st = it % NS;
+          if (it >= NS && !warp_wait(empty + st, ((it / NS) - 1) & 1, abort_flag, a.status)) {
+            stop = true;
+            break;
+          }
+          if (lane == 0) mbar_expect_tx(full + st, nops * 512);
+          __syncwarp();
+          if (active)
+            tma_gather4(ring + st * L::kTileBytes + sub * L::kSubBytes + quad * 4 * 128,
+                        kv ? &tv : &tk, sub * 64, r[0], r[1], r[2], r[3], full + st);
+          ++issued;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          cur[i] = nxt[i];
+          nxt[i] = ahead[i];
+        }
       }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
-      if (*abort_flag) {
-        if (k_issued) drain_wait(k_full, (k_issued - 1) & 1);
-        if (v_issued) drain_wait(v_full, (v_issued - 1) & 1);
+      if (*abort_flag && lane == 0) {
+        // let this warp's copies land before the CTA exits
+        for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
+          drain_wait(full + (it % NS), (it / NS) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
-      const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk), v_addr = smem_u32(sv);
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.status);
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (!mbar_wait(k_full, j & 1, abort_flag, a.status)) break;
+      const uint32_t q_addr = smem_u32(sq), ring_addr = smem_u32(ring);
+      auto issue_qk = [&](int j) -> bool {
+        const int i = 2 * j, st = i % NS;
+        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
         tc_fence_after();
+        const uint32_t kb = ring_addr + st * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                  idesc_qk, kk > 0);
+          umma_ss(tmem + (j & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024),
+                  sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
         }
-        umma_commit(s_full);
-        umma_commit(k_empty);
-        if (!mbar_wait(p_full, j & 1, abort_flag, a.status)) break;
-        if (!mbar_wait(v_full, j & 1, abort_flag, a.status)) break;
+        umma_commit(s_full + (j & 1));
+        umma_commit(empty + st);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, a.status) && issue_qk(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        // S(j+1) goes into the other buffer, whose P(j-1) was consumed by
+        // PV(j-1), issued earlier (MMAs of one thread execute in order).
+        if (j + 1 < nkv && !issue_qk(j + 1)) break;
+        if (!mbar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) break;
+        const int i = 2 * j + 1, st = i % NS;
+        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) break;
         tc_fence_after();
+        const uint32_t vb = ring_addr + st * L::kTileBytes;
+        const uint32_t tP = tmem + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ts(tO, tS + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, L::kSubBytes, 1024),
-                  idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tO, tP + kk * 8, sdesc_sw128(vb + kk * 16 * 128, L::kSubBytes, 1024), idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(v_empty);
+        umma_commit(o_done);
+        umma_commit(empty + st);
       }
       umma_commit(o_full);
       drain_wait(o_full, 0);
@@ -234,12 +294,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!warp_wait(s_full, j & 1, abort_flag, a.status)) { ok = false; break; }
+      if (!warp_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t tS = tmem + (j & 1) * 128 + lane_off;
       float s[BN];
       uint32_t* su = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + lane_off + c * 32, su + c * 32);
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
       tmem_ld_wait();
       const int valid = kv_total - j * BN;
       if (valid < BN) {
@@ -247,17 +308,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < BN; ++c)
           if (c >= valid) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: four independent chains of 3-input max (short latency chain)
+      float mc0 = s[0], mc1 = s[1], mc2 = s[2], mc3 = s[3];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 4; c < BN; c += 8) {
+        mc0 = fmax3(mc0, s[c + 0], s[c + 1]);
+        mc1 = fmax3(mc1, s[c + 2], s[c + 3]);
+        mc2 = fmax3(mc2, s[c + 4 < BN ? c + 4 : 0], s[c + 5 < BN ? c + 5 : 0]);
+        mc3 = fmax3(mc3, s[c + 6 < BN ? c + 6 : 0], s[c + 7 < BN ? c + 7 : 0]);
+      }
+      const float mx = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3));
       const float m_new = mx * sl2;
       // Lazy rescaling: a row's reference max only moves when the tile max
       // exceeds it by more than the threshold.  TMEM loads/stores are
       // warp-collective, so the whole warp enters the rescale when any of its
-      // rows needs it (f = 1 for the others).
+      // rows needs it (f = 1 for the others).  O may still be accumulating
+      // PV(j-1): wait for it first (PV(j) cannot start before this P(j)).
       const bool need = (j > 0) && (m_new > m_run + kRescaleThreshold);
       if (j == 0) m_run = m_new;
       if (__any_sync(0xffffffffu, need)) {
+        if (!warp_wait(o_done, (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
         const float f = need ? ex2(m_run - m_new) : 1.f;
         l_f32 *= f;
         l_b16 *= f;
@@ -272,28 +343,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (need) m_run = m_new;
       }
-      float sum_f = 0.f, sum_b = 0.f;
+      // p = 2^(s*c - m): packed FFMA2 for the argument, MUFU ex2, bf16 pack.
+      // Two row sums, each in four packed accumulators: the fp32 weights (for
+      // the LSE) and the bf16 weights the PV product actually multiplies by
+      // (the output is normalised by those, which keeps its error smaller).
+      const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_run, -m_run);
+      uint64_t accf[4] = {0ull, 0ull, 0ull, 0ull}, accb[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, -m_run));
-          const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, -m_run));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
           pk[i] = pack_bf16(p0, p1);
-          sum_f += p0 + p1;
-          // the output is normalised by the sum of the bf16 weights the PV
-          // product actually uses; the LSE by the fp32 sum
-          sum_b += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          accf[i & 3] = f2_add(accf[i & 3], f2_pack(p0, p1));
+          accb[i & 3] = f2_add(accb[i & 3], f2_pack(__uint_as_float(pk[i] << 16),
+                                                    __uint_as_float(pk[i] & 0xFFFF0000u)));
         }
-        tmem_st16(tS + lane_off + c * 16, pk);
+        tmem_st16(tS + c * 16, pk);
       }
-      l_f32 += sum_f;
-      l_b16 += sum_b;
+      l_f32 += sum8(accf);
+      l_b16 += sum8(accb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full + (j & 1));
     }
     // ------------------------------------------------------------ epilogue
     if (ok && warp_wait(o_full, 0, abort_flag, a.status)) {
@@ -351,14 +427,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (MODE == kDense && a.lse != nullptr && token >= 0)
-        a.lse[static_cast<size_t>(bh) * a.N + token] = (m_run + __log2f(l_f32)) * 0.69314718055994531f;
+        a.lse[static_cast<size_t>(bh) * a.N + token] =
+            (m_run + __log2f(l_f32)) * 0.69314718055994531f;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 template <int D, int MODE>
