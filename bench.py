@@ -48,7 +48,10 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, with the
 # sha1 of the kernel source it was measured on (traffic is reported only
 # while the source is unchanged).  Filled from profiles/.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/dram_traffic_large.md: sparse reuse launch, full size
+    "attn.cu": {"sha": "0f3f09dd7ce6", "bytes_per_launch": 5057806848 + 831960064},
+}
 
 
 def _peaks():
