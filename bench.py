@@ -49,7 +49,7 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # sha1 of the kernel source it was measured on (traffic is reported only
 # while the source is unchanged).  Filled from profiles/.
 TRAFFIC = {
-    # profiles/dram_traffic_large.md: sparse reuse launch, full size
+    # measured with ncu on the full-size sparse reuse launch
     "attn.cu": {"sha": "0f3f09dd7ce6", "bytes_per_launch": 5057806848 + 831960064},
 }
 

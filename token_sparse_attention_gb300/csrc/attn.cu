@@ -14,10 +14,13 @@
 //   warps 0-3  softmax + epilogue: thread t owns query row t = TMEM lane t
 //   warps 4-10 producers: K and V tiles into a ring of kStages shared-memory
 //              stages, as far ahead as the ring allows.  Dense: one thread
-//              issues TMA tile loads.  Sparse: every K or V tile is 32*D/64
-//              TMA gather4 operations (4 rows x 64 columns each); they are
-//              spread over the 7 producer warps, one per lane, because the
-//              gather rate grows with the number of warps issuing them
+//              issues TMA tile loads.  Sparse: the 224 producer threads copy
+//              the indexed K/V rows with 16-byte cp.async (two whole 256-byte
+//              rows per warp instruction), writing them straight into the
+//              128-byte-swizzled layout the MMA reads; each thread arrives
+//              on the stage's mbarrier when its copies land.  (TMA gather4,
+//              used for the one-time Q tile, issues too slowly per warp to
+//              keep up with the tensor core here.)
 //   warp 11    TMEM allocation and the single MMA-issuing thread
 // TMEM (512 columns): two score buffers S0/S1 (128 fp32 columns each; P is
 // written over S as bf16 pairs) and the O accumulator.  The MMA order
@@ -34,6 +37,7 @@ namespace {
 constexpr int BM = 128;  // query rows per CTA (MMA M)
 constexpr int BN = 128;  // KV rows per tile (MMA N of QK^T, K of PV)
 constexpr int kProducers = 7;
+constexpr int kFirstProducer = 4;
 constexpr int kMmaWarp = 4 + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kRescaleThreshold = 8.0f;
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full + s, MODE == kDense ? 1 : kProducers);  // sparse: every producer warp
+      mbar_init(full + s, MODE == kDense ? 1 : 32 * kProducers);  // sparse: every producer thread
       mbar_init(empty + s, 1);
     }
     mbar_init(q_full, 1);
@@ -158,22 +162,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // Sparse.  Gather operation q in [0, 32*kSub) of a tile (sub-tile
-      // q / 32, rows 4*(q % 32) .. +3) is issued by producer warp q % 7,
-      // lane q / 7.
+      // Sparse.  Tile rows are token indices idx[j*128 + r]; a tile is
+      // kChunks 16-byte chunks (row r = c / kSegs, segment c % kSegs) and
+      // producer thread t copies chunks t, t + kPT, t + 2*kPT, ...
+      constexpr int kPT = 32 * kProducers;
+      constexpr int kSegs = D * 2 / 16;                 // 16-byte segments per row
+      constexpr int kChunks = BN * kSegs;
+      constexpr int kPer = (kChunks + kPT - 1) / kPT;   // chunks per thread (at most)
       const size_t grp = static_cast<size_t>(bh) * a.G + tile;
       const int32_t* perm_g = a.perm + grp * a.C;
       const int32_t* idx_g = a.idx + grp * a.K;
       const int rowbase = bh * a.N;
-      const int pw = warp - 4;                       // 0..kProducers-1
-      const int q = pw + kProducers * lane;          // this lane's operation
-      const bool active = q < 32 * L::kSub;
-      const int nops = (32 * L::kSub - pw + kProducers - 1) / kProducers;  // this warp's count
-      const int sub = q / 32;
-      const int quad = q % 32;
+      const int tid = (warp - kFirstProducer) * 32 + lane;
       bool bad = false;
-      int r[4];
-      if (warp == 4) {
+      if (warp == kFirstProducer) {
+        int r[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int p = 4 * lane + i;
@@ -184,8 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
           tma_prefetch_desc(&tq);
-          tma_prefetch_desc(&tk);
-          tma_prefetch_desc(&tv);
           mbar_expect_tx(q_full, L::kTileBytes);
         }
         __syncwarp();
@@ -193,28 +194,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_gather4(sq + s * L::kSubBytes + lane * 4 * 128, &tq, s * 64, r[0], r[1], r[2],
                       r[3], q_full);
       }
-      // Row indices of tile j are loaded two tiles ahead so their latency
-      // (the index array is read once, from HBM) stays off the critical path.
-      auto load_idx = [&](int j, int* out) {
+      // Token indices of this thread's rows, loaded two tiles ahead so that
+      // their latency (the index array is read once, from HBM) stays off the
+      // critical path.
+      auto load_rows = [&](int j, int* out) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int c = j * BN + 4 * quad + i;
-          c = c < a.K ? c : a.K - 1;  // tail columns repeat a valid row; masked in softmax
-          out[i] = active ? __ldg(idx_g + c) : 0;
+        for (int k = 0; k < kPer; ++k) {
+          const int c = tid + kPT * k;
+          int col = j * BN + (c < kChunks ? c / kSegs : 0);
+          col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked in softmax
+          out[k] = __ldg(idx_g + col);
         }
       };
-      int cur[4], nxt[4] = {0, 0, 0, 0};
-      load_idx(0, cur);
-      if (nkv > 1) load_idx(1, nxt);
+      int cur[kPer], nxt[kPer];
+      load_rows(0, cur);
+      if (nkv > 1) load_rows(1, nxt);
       bool stop = false;
       for (int j = 0; j < nkv && !stop; ++j) {
-        int ahead[4] = {0, 0, 0, 0};
-        if (j + 2 < nkv) load_idx(j + 2, ahead);
+        int ahead[kPer];
+        if (j + 2 < nkv) load_rows(j + 2, ahead);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int t = cur[i];
-          if (t < 0 || t >= a.N) { bad = true; t = 0; }
-          r[i] = rowbase + t;
+        for (int k = 0; k < kPer; ++k) {
+          if (cur[k] < 0 || cur[k] >= a.N) { bad = true; cur[k] = 0; }
         }
         for (int kv = 0; kv < 2; ++kv) {
           const int it = 2 * j + kv;
@@ -223,25 +224,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          if (lane == 0) mbar_expect_tx(full + st, nops * 512);
-          __syncwarp();
-          if (active)
-            tma_gather4(ring + st * L::kTileBytes + sub * L::kSubBytes + quad * 4 * 128,
-                        kv ? &tv : &tk, sub * 64, r[0], r[1], r[2], r[3], full + st);
+          const __nv_bfloat16* src = kv ? a.v : a.k;
+          uint8_t* stage = ring + st * L::kTileBytes;
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int c = tid + kPT * k;
+            if (c < kChunks) {
+              const int r = c / kSegs, seg = c % kSegs;
+              uint8_t* dst = stage + (seg >> 3) * L::kSubBytes + r * 128 +
+                             (((seg & 7) ^ (r & 7)) << 4);
+              cp_async16(dst, src + static_cast<size_t>(rowbase + cur[k]) * D + seg * 8);
+            }
+          }
+          cp_async_arrive(full + st);
           ++issued;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          cur[i] = nxt[i];
-          nxt[i] = ahead[i];
+        for (int k = 0; k < kPer; ++k) {
+          cur[k] = nxt[k];
+          nxt[k] = ahead[k];
         }
       }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
-      if (*abort_flag && lane == 0) {
-        // let this warp's copies land before the CTA exits
-        for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
-          drain_wait(full + (it % NS), (it / NS) & 1);
-      }
+      if (*abort_flag) asm volatile("cp.async.wait_all;" ::: "memory");  // copies land first
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -252,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_qk = [&](int j) -> bool {
         const int i = 2 * j, st = i % NS;
         if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
+        if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
         tc_fence_after();
         const uint32_t kb = ring_addr + st * L::kTileBytes;
 #pragma unroll
@@ -272,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) break;
         const int i = 2 * j + 1, st = i % NS;
         if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) break;
+        if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
         tc_fence_after();
         const uint32_t vb = ring_addr + st * L::kTileBytes;
         const uint32_t tP = tmem + (j & 1) * 128;

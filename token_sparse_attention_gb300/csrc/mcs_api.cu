@@ -123,6 +123,8 @@ mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const v
   a.perm = perm;
   a.idx = idx;
   a.aux_in = static_cast<const __nv_bfloat16*>(aux);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
   cudaError_t e = mcs::launch_attention(p->D, mode, &tq, &tk, &tv, a, BH, stream);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");

@@ -106,6 +106,19 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// 16-byte global -> shared copy through the LSU (L2 only), asynchronous.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this thread).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
