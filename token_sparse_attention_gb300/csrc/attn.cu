@@ -47,9 +47,8 @@ struct AttnLayout {
   static constexpr int kSub = D / 64;          // 128-byte column sub-tiles per row
   static constexpr int kSubBytes = 128 * 128;  // one sub-tile: 128 rows x 128 B
   static constexpr int kTileBytes = kSub * kSubBytes;
-  static constexpr int kStages = D == 128 ? 6 : 12;  // K/V ring depth (tiles)
-  static constexpr int kQ = 0;
-  static constexpr int kRing = kTileBytes;
+  static constexpr int kStages = D == 128 ? 7 : 14;  // K/V ring depth (tiles)
+  static constexpr int kRing = 0;
   static constexpr int kBars = kRing + kStages * kTileBytes;
   static constexpr int kNumBars = 2 * kStages + 7;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
@@ -89,12 +88,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sq = smem + L::kQ;
   uint8_t* ring = smem + L::kRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* full = bars;              // [NS] stage loaded
   uint64_t* empty = bars + NS;        // [NS] stage consumed by its MMA
-  uint64_t* q_full = bars + 2 * NS;
+  uint64_t* q_full = bars + 2 * NS;   // Q tile written to TMEM (4 warp arrivals)
   uint64_t* s_full = q_full + 1;      // [2] S(j) in buffer j&1 computed
   uint64_t* p_full = q_full + 3;      // [2] P(j) written (4 warp arrivals)
   uint64_t* o_done = q_full + 5;      // PV(j) complete
@@ -114,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full + s, MODE == kDense ? 1 : 32 * kProducers);  // sparse: every producer thread
       mbar_init(empty + s, 1);
     }
-    mbar_init(q_full, 1);
+    mbar_init(q_full, 4);
     mbar_init(s_full + 0, 1);
     mbar_init(s_full + 1, 1);
     mbar_init(p_full + 0, 4);
@@ -132,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 256;  // S0 at +0, S1 at +128
+  const uint32_t tO = tmem + 256;      // S0 at +0, S1 at +128
+  const uint32_t tQ = tmem + 256 + D;  // Q tile, bf16 pairs (D/2 columns)
 
   if (warp >= 4 && warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
@@ -140,12 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if (MODE == kDense) {
       if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
-        mbar_expect_tx(q_full, L::kTileBytes);
-        for (int s = 0; s < L::kSub; ++s)
-          tma_load_3d(sq + s * L::kSubBytes, &tq, s * 64, tile * BM, bh, q_full);
         for (int i = 0; i < 2 * nkv; ++i) {
           const int st = i % NS;
           if (i >= NS && !mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
@@ -170,30 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kChunks = BN * kSegs;
       constexpr int kPer = (kChunks + kPT - 1) / kPT;   // chunks per thread (at most)
       const size_t grp = static_cast<size_t>(bh) * a.G + tile;
-      const int32_t* perm_g = a.perm + grp * a.C;
       const int32_t* idx_g = a.idx + grp * a.K;
       const int rowbase = bh * a.N;
       const int tid = (warp - kFirstProducer) * 32 + lane;
       bool bad = false;
-      if (warp == kFirstProducer) {
-        int r[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = 4 * lane + i;
-          int t = (p < a.C) ? __ldg(perm_g + p) : 0;
-          if (t < 0) t = 0;  // padding slot of the short last group
-          if (t >= a.N) { bad = true; t = 0; }
-          r[i] = rowbase + t;
-        }
-        if (lane == 0) {
-          tma_prefetch_desc(&tq);
-          mbar_expect_tx(q_full, L::kTileBytes);
-        }
-        __syncwarp();
-        for (int s = 0; s < L::kSub; ++s)
-          tma_gather4(sq + s * L::kSubBytes + lane * 4 * 128, &tq, s * 64, r[0], r[1], r[2],
-                      r[3], q_full);
-      }
       // Token indices of this thread's rows, loaded two tiles ahead so that
       // their latency (the index array is read once, from HBM) stays off the
       // critical path.
@@ -253,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
-      const uint32_t q_addr = smem_u32(sq), ring_addr = smem_u32(ring);
+      const uint32_t ring_addr = smem_u32(ring);
       auto issue_qk = [&](int j) -> bool {
         const int i = 2 * j, st = i % NS;
         if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
@@ -261,10 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t kb = ring_addr + st * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {  // A = Q from TMEM, B = K tile
           const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
-          umma_ss(tmem + (j & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                  sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+          umma_ts(tmem + (j & 1) * 128, tQ + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_qk,
+                  kk > 0);
         }
         umma_commit(s_full + (j & 1));
         umma_commit(empty + st);
@@ -300,6 +275,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
+    {
+      // Q tile -> TMEM (the QK MMA's A operand, read from TMEM every tile
+      // instead of shared memory): row `row` holds its D bf16 values as D/2
+      // 32-bit columns, lower index in the low half.  Missing rows are zero.
+      int src = -1;
+      if (MODE == kDense) {
+        src = tile * BM + row;
+        if (src >= a.N) src = -1;
+      } else if (row < a.C) {
+        src = __ldg(a.perm + (static_cast<size_t>(bh) * a.G + tile) * a.C + row);
+        if (src >= a.N) {
+          atomicOr(a.status, DEV_BOUNDS);
+          src = -1;
+        }
+      }
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(bh) * a.N + (src < 0 ? 0 : src)) * D);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {  // 32 columns (64 values) at a time
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = src >= 0 ? __ldg(qrow + c * 8 + i) : make_uint4(0, 0, 0, 0);
+          w[4 * i + 0] = x.x;
+          w[4 * i + 1] = x.y;
+          w[4 * i + 2] = x.z;
+          w[4 * i + 3] = x.w;
+        }
+        tmem_st32(tQ + lane_off + c * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
     for (int j = 0; j < nkv; ++j) {
       if (!warp_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
       tc_fence_after();

@@ -34,6 +34,7 @@ struct AttnArgs {
   const int32_t* perm;           // [BH, G*C]
   const int32_t* idx;            // [BH, G, K]
   const __nv_bfloat16* aux_in;   // kSparseAdd: residual; kSparseRecord: dense_out
+  const __nv_bfloat16* q;        // [BH, N, D] (rows of the query tile / group)
   const __nv_bfloat16* k;        // [BH, N, D] (sparse modes: rows gathered by idx)
   const __nv_bfloat16* v;        // [BH, N, D]
   unsigned* status;              // device status word

@@ -123,6 +123,7 @@ mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const v
   a.perm = perm;
   a.idx = idx;
   a.aux_in = static_cast<const __nv_bfloat16*>(aux);
+  a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
@@ -234,6 +235,9 @@ mcs_status mcs_dense_attn(const mcs_params* p, const void* q, const void* k, con
   a.scale_log2 = scale_of(p) * kLog2e;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
   cudaError_t e = mcs::launch_attention(p->D, mcs::kDense, &tq, &tk, &tv, a, BH, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dense attention launch");
