@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         for (int i = 0; i < 2 * nkv; ++i) {
+          if (a.fault && i >= 2) break;  // test-only: starve the MMA thread
           const int st = i % NS;
           if (i >= NS && !mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
           mbar_expect_tx(full + st, L::kTileBytes);
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nkv > 1) load_rows(1, nxt);
       bool stop = false;
       for (int j = 0; j < nkv && !stop; ++j) {
+        if (a.fault && j >= 1) break;  // test-only: starve the MMA thread
         int ahead[kPer];
         if (j + 2 < nkv) load_rows(j + 2, ahead);
 #pragma unroll

@@ -38,6 +38,7 @@ struct AttnArgs {
   const __nv_bfloat16* k;        // [BH, N, D] (sparse modes: rows gathered by idx)
   const __nv_bfloat16* v;        // [BH, N, D]
   unsigned* status;              // device status word
+  int fault;                     // test-only: 1 = producers stop after the first K/V tile
 };
 
 // tq/tk/tv: dense -> 3-D tile maps [BH][N][D], box {64,128,1};

@@ -3,6 +3,7 @@
 // include/mcs.h.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -97,6 +98,15 @@ mcs_status status_ptr(unsigned** out) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Test-only fault injection for the attention kernels: with the environment
+// variable MCS_TEST_FAULT=stall_load the producers stop after the first K/V
+// tile, so the MMA thread's next bounded wait expires (MCS_ERR_TIMEOUT) and
+// the kernel's teardown path runs.  Read at every call; unset in normal use.
+int fault_from_env() {
+  const char* f = getenv("MCS_TEST_FAULT");
+  return (f != nullptr && strcmp(f, "stall_load") == 0) ? 1 : 0;
+}
+
 mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const void* v,
                       const int32_t* perm, const int32_t* idx, const void* aux, void* out,
                       int mode, cudaStream_t stream) {
@@ -126,6 +136,7 @@ mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const v
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
+  a.fault = fault_from_env();
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
   cudaError_t e = mcs::launch_attention(p->D, mode, &tq, &tk, &tv, a, BH, stream);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
@@ -238,6 +249,7 @@ mcs_status mcs_dense_attn(const mcs_params* p, const void* q, const void* k, con
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
+  a.fault = fault_from_env();
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
   cudaError_t e = mcs::launch_attention(p->D, mcs::kDense, &tq, &tk, &tv, a, BH, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dense attention launch");
