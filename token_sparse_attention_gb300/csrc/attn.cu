@@ -138,18 +138,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Ring item i = 2j (K tile j) or 2j+1 (V tile j) goes to stage i % NS.
     int issued = 0;
     if (MODE == kDense) {
-      if (warp == 4 && lane == 0) {
+      if (warp == 4) {  // the whole warp waits; an elected lane issues the loads
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         for (int i = 0; i < 2 * nkv; ++i) {
           if (a.fault && i >= 2) break;  // test-only: starve the MMA thread
           const int st = i % NS;
-          if (i >= NS && !mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
-          mbar_expect_tx(full + st, L::kTileBytes);
-          const CUtensorMap* tm = (i & 1) ? &tv : &tk;
-          uint8_t* dst = ring + st * L::kTileBytes;
-          for (int s = 0; s < L::kSub; ++s)
-            tma_load_3d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, bh, full + st);
+          if (i >= NS && !warp_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
+          if (elect_one()) {
+            mbar_expect_tx(full + st, L::kTileBytes);
+            const CUtensorMap* tm = (i & 1) ? &tv : &tk;
+            uint8_t* dst = ring + st * L::kTileBytes;
+            for (int s = 0; s < L::kSub; ++s)
+              tma_load_3d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, bh, full + st);
+          }
+          __syncwarp();
           ++issued;
         }
         if (*abort_flag) {
@@ -227,16 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
-      const uint32_t ring_addr = smem_u32(ring);
-      auto issue_qk = [&](int j) -> bool {
-        const int i = 2 * j, st = i % NS;
-        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
-        if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
-        tc_fence_after();
-        const uint32_t kb = ring_addr + st * L::kTileBytes;
+    // The whole warp runs the loop (every branch warp-uniform) and one lane,
+    // chosen by elect.sync right before each batch, issues the MMAs.  Issuing
+    // from a lane-0-only branch instead is several times slower per MMA
+    // (measured: 8 MMAs took ~400 cycles to issue from a divergent branch,
+    // 69 from an elected lane), too slow to keep the tensor core fed.
+    constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
+    const uint32_t ring_addr = smem_u32(ring);
+    auto issue_qk = [&](int j) -> bool {
+      const int i = 2 * j, st = i % NS;
+      if (!warp_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
+      if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
+      tc_fence_after();
+      const uint32_t kb = ring_addr + st * L::kTileBytes;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {  // A = Q from TMEM, B = K tile
           const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
@@ -245,20 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(s_full + (j & 1));
         umma_commit(empty + st);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.status) && issue_qk(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        // S(j+1) goes into the other buffer, whose P(j-1) was consumed by
-        // PV(j-1), issued earlier (MMAs of one thread execute in order).
-        if (j + 1 < nkv && !issue_qk(j + 1)) break;
-        if (!mbar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) break;
-        const int i = 2 * j + 1, st = i % NS;
-        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag, a.status)) break;
-        if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
-        tc_fence_after();
-        const uint32_t vb = ring_addr + st * L::kTileBytes;
-        const uint32_t tP = tmem + (j & 1) * 128;
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = warp_wait(q_full, 0, abort_flag, a.status) && issue_qk(0);
+    for (int j = 0; ok && j < nkv; ++j) {
+      // S(j+1) goes into the other buffer, whose P(j-1) was consumed by
+      // PV(j-1), issued earlier (MMAs of one thread execute in order).
+      if (j + 1 < nkv && !issue_qk(j + 1)) break;
+      if (!warp_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) break;
+      const int i = 2 * j + 1, st = i % NS;
+      if (!warp_wait(full + st, (i / NS) & 1, abort_flag, a.status)) break;
+      if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
+      tc_fence_after();
+      const uint32_t vb = ring_addr + st * L::kTileBytes;
+      const uint32_t tP = tmem + (j & 1) * 128;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           umma_ts(tO, tP + kk * 8, sdesc_sw128(vb + kk * 16 * 128, L::kSubBytes, 1024), idesc_pv,
@@ -267,9 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(o_done);
         umma_commit(empty + st);
       }
-      umma_commit(o_full);
-      drain_wait(o_full, 0);
+      __syncwarp();
     }
+    if (elect_one()) umma_commit(o_full);
+    __syncwarp();
+    drain_wait(o_full, 0);
   } else {
     // ------------------------------------------------------------ softmax
     const int row = threadIdx.x;  // 0..127 == TMEM lane
