@@ -49,8 +49,9 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # sha1 of the kernel source it was measured on (traffic is reported only
 # while the source is unchanged).  Filled from profiles/.
 TRAFFIC = {
-    # measured with ncu on the full-size sparse reuse launch
-    "attn.cu": {"sha": "0f3f09dd7ce6", "bytes_per_launch": 5057806848 + 831960064},
+    # ncu dram bytes (read + write) of the sparse reuse launch of the 4-head
+    # large workload, times 10 for the 40-head launch (heads are independent)
+    "attn.cu": {"sha": "fa774a25284c", "bytes_per_launch": 10 * (625954048 + 68949760)},
 }
 
 

@@ -9,36 +9,42 @@
 // attention with row LSE is the selector's first pass (ai.info AI summary,
 // "Methodology in Plain English") and the speedup denominator.
 //
-// One CTA per SM; one CTA = one 128-row query tile (dense) or one query group
-// (sparse) of one head.
-//   warps 0-3  softmax + epilogue: thread t owns query row t = TMEM lane t
-//   warps 4-10 producers: K and V tiles into a ring of kStages shared-memory
-//              stages, as far ahead as the ring allows.  Dense: one thread
-//              issues TMA tile loads.  Sparse: the 224 producer threads copy
-//              the indexed K/V rows with 16-byte cp.async (two whole 256-byte
-//              rows per warp instruction), writing them straight into the
-//              128-byte-swizzled layout the MMA reads; each thread arrives
-//              on the stage's mbarrier when its copies land.  (TMA gather4,
-//              used for the one-time Q tile, issues too slowly per warp to
-//              keep up with the tensor core here.)
-//   warp 11    TMEM allocation and the single MMA-issuing thread
-// TMEM (512 columns): two score buffers S0/S1 (128 fp32 columns each; P is
-// written over S as bf16 pairs) and the O accumulator.  The MMA order
-//   QK(0), QK(1), PV(0), QK(2), PV(1), QK(3), ...
-// lets the tensor core compute S(j+1) and PV(j-1) while the softmax warps
-// work on S(j).  Online softmax in base 2 with lazy rescaling (O is rescaled
-// only when a row's running max grows by more than 8, so P <= 256).
+// One CTA per SM works on TWO query units of one head at once, a and b:
+// query tiles 2x and 2x+1 (dense) or query groups 2x and 2x+1 (sparse).  The
+// two units form independent softmax -> PV -> QK chains, so the tensor core
+// runs one unit's products while the other unit's softmax warps work; with a
+// single unit per CTA the softmax, the MMA completion latency and the
+// hand-offs of every tile sat on the critical path.
+//   warps 0-3   softmax + epilogue of unit a; thread t owns query row t
+//   warps 4-7   the same for unit b
+//   warps 8-14  producers.  Dense: one warp issues TMA tile loads of Q and of
+//               the K/V tiles both units share.  Sparse: the 224 producer
+//               threads copy each unit's query rows (by perm) and indexed K/V
+//               rows (by idx) with 16-byte cp.async straight into the
+//               128-byte-swizzled layout the MMA reads, and arrive on the
+//               stage's mbarrier when their copies land.
+//   warp 15     TMEM allocation and MMA issue (one elected lane)
+// Shared memory: Q_a and Q_b (the QK A-operands) and a ring of K/V tiles.
+// TMEM (512 columns): S_a, S_b (128 fp32 columns each; P is written over S
+// as bf16 pairs) and the accumulators O_a, O_b.  MMA order
+//   QK_a(0) QK_b(0) | PV_a(0) QK_a(1) PV_b(0) QK_b(1) | PV_a(1) QK_a(2) ...
+// QK_x(j+1) overwrites S_x only after PV_x(j), which read P_x(j), in the
+// in-order MMA stream; and a commit signals completion of every earlier MMA,
+// so a softmax warp that sees S_x(j) complete knows PV_x(j-1) is done too.
+// Online softmax in base 2 with lazy rescaling (O is rescaled only when a
+// row's running max grows by more than 8, so P <= 256).
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace mcs {
 namespace {
 
-constexpr int BM = 128;  // query rows per CTA (MMA M)
+constexpr int BM = 128;  // query rows per unit (MMA M)
 constexpr int BN = 128;  // KV rows per tile (MMA N of QK^T, K of PV)
+constexpr int kSoftmaxWarps = 8;
 constexpr int kProducers = 7;
-constexpr int kFirstProducer = 4;
-constexpr int kMmaWarp = 4 + kProducers;
+constexpr int kFirstProducer = kSoftmaxWarps;
+constexpr int kMmaWarp = kFirstProducer + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -46,9 +52,10 @@ template <int D>
 struct AttnLayout {
   static constexpr int kSub = D / 64;          // 128-byte column sub-tiles per row
   static constexpr int kSubBytes = 128 * 128;  // one sub-tile: 128 rows x 128 B
-  static constexpr int kTileBytes = kSub * kSubBytes;
-  static constexpr int kStages = D == 128 ? 7 : 14;  // K/V ring depth (tiles)
-  static constexpr int kRing = 0;
+  static constexpr int kTileBytes = kSub * kSubBytes;  // a 128-row tile of Q, K or V
+  static constexpr int kStages = D == 128 ? 5 : 12;    // K/V ring depth (tiles)
+  static constexpr int kQ = 0;                         // Q_a, Q_b
+  static constexpr int kRing = 2 * kTileBytes;
   static constexpr int kBars = kRing + kStages * kTileBytes;
   static constexpr int kNumBars = 2 * kStages + 7;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
@@ -79,46 +86,79 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Max of 64 scores: four independent chains of 3-input max.
+__device__ __forceinline__ float max64(const float* s) {
+  float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+  for (int c = 4; c < 60; c += 8) {
+    m0 = fmax3(m0, s[c + 0], s[c + 1]);
+    m1 = fmax3(m1, s[c + 2], s[c + 3]);
+    m2 = fmax3(m2, s[c + 4], s[c + 5]);
+    m3 = fmax3(m3, s[c + 6], s[c + 7]);
+  }
+  m0 = fmax3(m0, s[60], s[61]);
+  m1 = fmax3(m1, s[62], s[63]);
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// Byte offset of 16-byte chunk `seg` of row r in a 128-row tile stored as
+// 128-byte-swizzled K-major sub-tiles (the layout TMA writes with SW128).
+__device__ __forceinline__ int swz_offset(int r, int seg) {
+  return (seg >> 3) * (128 * 128) + r * 128 + (((seg & 7) ^ (r & 7)) << 4);
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
   using L = AttnLayout<D>;
   constexpr int NS = L::kStages;
+  constexpr bool kSparseMode = MODE != kDense;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  uint8_t* qs = smem + L::kQ;  // Q_a, then Q_b
   uint8_t* ring = smem + L::kRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* full = bars;              // [NS] stage loaded
-  uint64_t* empty = bars + NS;        // [NS] stage consumed by its MMA
-  uint64_t* q_full = bars + 2 * NS;   // Q tile written to TMEM (4 warp arrivals)
-  uint64_t* s_full = q_full + 1;      // [2] S(j) in buffer j&1 computed
-  uint64_t* p_full = q_full + 3;      // [2] P(j) written (4 warp arrivals)
-  uint64_t* o_done = q_full + 5;      // PV(j) complete
-  uint64_t* o_full = q_full + 6;      // every MMA complete
+  uint64_t* empty = bars + NS;        // [NS] stage consumed by its last MMA
+  uint64_t* q_full = bars + 2 * NS;   // Q_a and Q_b loaded
+  uint64_t* s_full = q_full + 1;      // [2] S_x(j) computed
+  uint64_t* p_full = q_full + 3;      // [2] P_x(j) written (4 warp arrivals)
+  uint64_t* o_full = q_full + 5;      // [2] every PV of unit x complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int tile = blockIdx.x;
+  const int pair = blockIdx.x;
   const int bh = blockIdx.y;
-  const int kv_total = (MODE == kDense) ? a.N : a.K;
+  const int units = kSparseMode ? a.G : (a.N + BM - 1) / BM;  // units per head
+  const bool has_b = 2 * pair + 1 < units;
+  const int kv_total = kSparseMode ? a.K : a.N;
   const int nkv = (kv_total + BN - 1) / BN;
+  // Ring items, numbered in the order the MMA warp consumes them (item i
+  // goes to stage i % NS).  Dense: K(j) = 2j, V(j) = 2j+1, each shared by
+  // both units.  Sparse: K_a(0) = 0, K_b(0) = 1, then per step j
+  // V_a(j) = 4j+2, K_a(j+1) = 4j+3, V_b(j) = 4j+4, K_b(j+1) = 4j+5 (the two
+  // K items of the last step do not exist).  In consumption order, every
+  // gather has the same lead: the NS - 1 products before it.
+  auto k_item = [&](int x, int j) {
+    return kSparseMode ? (j == 0 ? x : 4 * j - 1 + 2 * x) : 2 * j;
+  };
+  auto v_item = [&](int x, int j) { return kSparseMode ? 4 * j + 2 + 2 * x : 2 * j + 1; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full + s, MODE == kDense ? 1 : 32 * kProducers);  // sparse: every producer thread
+      mbar_init(full + s, kSparseMode ? 32 * kProducers : 1);  // sparse: every producer thread
       mbar_init(empty + s, 1);
     }
-    mbar_init(q_full, 4);
-    mbar_init(s_full + 0, 1);
-    mbar_init(s_full + 1, 1);
-    mbar_init(p_full + 0, 4);
-    mbar_init(p_full + 1, 4);
-    mbar_init(o_done, 1);
-    mbar_init(o_full, 1);
+    mbar_init(q_full, kSparseMode ? 32 * kProducers : 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full + x, 1);
+      mbar_init(p_full + x, 4);
+      mbar_init(o_full + x, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -129,20 +169,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 256;      // S0 at +0, S1 at +128
-  const uint32_t tQ = tmem + 256 + D;  // Q tile, bf16 pairs (D/2 columns)
+  const uint32_t tmem = *tmem_slot;  // S_a at +0, S_b at +128, O_a at +256, O_b at +256+D
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= kFirstProducer && warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // Ring item i = 2j (K tile j) or 2j+1 (V tile j) goes to stage i % NS.
     int issued = 0;
-    if (MODE == kDense) {
-      if (warp == 4) {  // the whole warp waits; an elected lane issues the loads
+    if (!kSparseMode) {
+      if (warp == kFirstProducer) {  // the whole warp waits; an elected lane issues the loads
+        tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
+        if (elect_one()) {
+          // Q_a, Q_b: rows past N (and a missing unit b) are zero-filled by TMA
+          mbar_expect_tx(q_full, 2 * L::kTileBytes);
+          for (int x = 0; x < 2; ++x)
+            for (int s = 0; s < L::kSub; ++s)
+              tma_load_3d(qs + x * L::kTileBytes + s * L::kSubBytes, &tq, s * 64,
+                          (2 * pair + x) * BM, bh, q_full);
+        }
+        __syncwarp();
         for (int i = 0; i < 2 * nkv; ++i) {
-          if (a.fault && i >= 2) break;  // test-only: starve the MMA thread
+          if (a.fault && i >= 2) break;  // test-only: starve the MMA warp
           const int st = i % NS;
           if (i >= NS && !warp_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
           if (elect_one()) {
@@ -152,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < L::kSub; ++s)
               tma_load_3d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, bh, full + st);
           }
-          __syncwarp();
           ++issued;
         }
         if (*abort_flag) {
@@ -161,68 +207,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // Sparse.  Tile rows are token indices idx[j*128 + r]; a tile is
-      // kChunks 16-byte chunks (row r = c / kSegs, segment c % kSegs) and
-      // producer thread t copies chunks t, t + kPT, t + 2*kPT, ...
+      // Sparse.  A tile is kChunks 16-byte chunks (row r = c / kSegs,
+      // segment c % kSegs); producer thread p copies chunks p, p + kPT, ...
       constexpr int kPT = 32 * kProducers;
       constexpr int kSegs = D * 2 / 16;                 // 16-byte segments per row
-      constexpr int kChunks = BN * kSegs;
+      constexpr int kChunks = BM * kSegs;
       constexpr int kPer = (kChunks + kPT - 1) / kPT;   // chunks per thread (at most)
-      const size_t grp = static_cast<size_t>(bh) * a.G + tile;
-      const int32_t* idx_g = a.idx + grp * a.K;
-      const int rowbase = bh * a.N;
       const int tid = (warp - kFirstProducer) * 32 + lane;
+      const int group[2] = {2 * pair, has_b ? 2 * pair + 1 : 2 * pair};
       bool bad = false;
-      // Token indices of this thread's rows, loaded two tiles ahead so that
-      // their latency (the index array is read once, from HBM) stays off the
-      // critical path.
-      auto load_rows = [&](int j, int* out) {
+      // Q rows of both units (perm order); padding slots, rows >= C and a
+      // missing unit b are zero rows.
+      for (int x = 0; x < 2; ++x) {
+        const int32_t* perm_g = a.perm + (static_cast<size_t>(bh) * a.G + group[x]) * a.C;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int c = tid + kPT * k;
+          if (c < kChunks) {
+            const int r = c / kSegs, seg = c % kSegs;
+            int tok = (r < a.C && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
+            if (tok >= a.N) { bad = true; tok = -1; }
+            const __nv_bfloat16* src =
+                a.q + (static_cast<size_t>(bh) * a.N + (tok < 0 ? 0 : tok)) * D + seg * 8;
+            cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, seg), src, tok >= 0);
+          }
+        }
+      }
+      cp_async_arrive(q_full);
+      // Global rows (b*H+h)*N + token of this thread's chunks of tile j of
+      // unit x; loaded two tiles ahead so that the index latency (the index
+      // array is read once, from HBM) stays off the critical path.
+      auto load_rows = [&](int x, int j, int* out) {
+        const int32_t* idx_g = a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int c = tid + kPT * k;
           int col = j * BN + (c < kChunks ? c / kSegs : 0);
           col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked in softmax
-          out[k] = __ldg(idx_g + col);
+          int tok = __ldg(idx_g + col);
+          if (tok < 0 || tok >= a.N) { bad = true; tok = 0; }
+          out[k] = bh * a.N + tok;
         }
       };
-      int cur[kPer], nxt[kPer];
-      load_rows(0, cur);
-      if (nkv > 1) load_rows(1, nxt);
-      bool stop = false;
-      for (int j = 0; j < nkv && !stop; ++j) {
-        if (a.fault && j >= 1) break;  // test-only: starve the MMA thread
-        int ahead[kPer];
-        if (j + 2 < nkv) load_rows(j + 2, ahead);
+      // Copy the rows of one K or V tile into the stage of ring item `it`.
+      auto copy_tile = [&](int it, const __nv_bfloat16* src, const int* rows) -> bool {
+        const int st = it % NS;
+        if (it >= NS && !warp_wait(empty + st, ((it / NS) - 1) & 1, abort_flag, a.status))
+          return false;
+        uint8_t* stage = ring + st * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-          if (cur[k] < 0 || cur[k] >= a.N) { bad = true; cur[k] = 0; }
-        }
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * j + kv;
-          const int st = it % NS;
-          if (it >= NS && !warp_wait(empty + st, ((it / NS) - 1) & 1, abort_flag, a.status)) {
-            stop = true;
-            break;
+          const int c = tid + kPT * k;
+          if (c < kChunks) {
+            const int r = c / kSegs, seg = c % kSegs;
+            cp_async16(stage + swz_offset(r, seg), src + static_cast<size_t>(rows[k]) * D + seg * 8);
           }
-          const __nv_bfloat16* src = kv ? a.v : a.k;
-          uint8_t* stage = ring + st * L::kTileBytes;
-#pragma unroll
-          for (int k = 0; k < kPer; ++k) {
-            const int c = tid + kPT * k;
-            if (c < kChunks) {
-              const int r = c / kSegs, seg = c % kSegs;
-              uint8_t* dst = stage + (seg >> 3) * L::kSubBytes + r * 128 +
-                             (((seg & 7) ^ (r & 7)) << 4);
-              cp_async16(dst, src + static_cast<size_t>(rowbase + cur[k]) * D + seg * 8);
-            }
-          }
-          cp_async_arrive(full + st);
-          ++issued;
         }
+        cp_async_arrive(full + st);
+        ++issued;
+        return true;
+      };
+      // rows of tiles j (V_x(j)), j+1 (K_x(j+1)) and j+2 (being fetched)
+      int r0[2][kPer], r1[2][kPer], r2[2][kPer];
+      load_rows(0, 0, r0[0]);
+      load_rows(1, 0, r0[1]);
+      if (nkv > 1) {
+        load_rows(0, 1, r1[0]);
+        load_rows(1, 1, r1[1]);
+      }
+      bool ok = copy_tile(k_item(0, 0), a.k, r0[0]) && copy_tile(k_item(1, 0), a.k, r0[1]);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (a.fault && j >= 1) break;  // test-only: starve the MMA warp
+        const bool more = j + 1 < nkv;
+        if (j + 2 < nkv) {
+          load_rows(0, j + 2, r2[0]);
+          load_rows(1, j + 2, r2[1]);
+        }
+        for (int x = 0; ok && x < 2; ++x)
+          ok = copy_tile(v_item(x, j), a.v, r0[x]) && (!more || copy_tile(k_item(x, j + 1), a.k, r1[x]));
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-          cur[k] = nxt[k];
-          nxt[k] = ahead[k];
+          r0[0][k] = r1[0][k];
+          r0[1][k] = r1[1][k];
+          r1[0][k] = r2[0][k];
+          r1[1][k] = r2[1][k];
         }
       }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
@@ -231,147 +299,163 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (every branch warp-uniform) and one lane,
-    // chosen by elect.sync right before each batch, issues the MMAs.  Issuing
-    // from a lane-0-only branch instead is several times slower per MMA
-    // (measured: 8 MMAs took ~400 cycles to issue from a divergent branch,
-    // 69 from an elected lane), too slow to keep the tensor core fed.
+    // chosen by elect.sync right before each batch, issues the MMAs; issuing
+    // from a lane-0-only branch is several times slower per MMA.
+    //
+    // The first mbarrier operation after a batch stalls until the tensor core
+    // has taken nearly the whole batch (it buffers only one or two MMAs), so
+    // a wait between batches is time the tensor core may sit idle.
+    //  Dense: per step the issuer waits for the step's K/V tiles at once (TMA
+    //    loads them well ahead), then issues PV_x(j) and QK_x(j+1) of a unit
+    //    as one batch, so that only the waits for P_a(j) and P_b(j) fall
+    //    between batches.
+    //  Sparse: each product waits only for its own operand and is issued on
+    //    its own: the gathered rows arrive just in time in the shallower ring
+    //    (four tiles per step), and tying PV_x(j) to the later K_x(j+1)
+    //    gather would hold it back.
     constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
     const uint32_t ring_addr = smem_u32(ring);
-    auto issue_qk = [&](int j) -> bool {
-      const int i = 2 * j, st = i % NS;
-      if (!warp_wait(full + st, (i / NS) & 1, abort_flag, a.status)) return false;
-      if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
-      tc_fence_after();
-      const uint32_t kb = ring_addr + st * L::kTileBytes;
-      if (elect_one()) {
+    const uint32_t q_addr = smem_u32(qs);
+    auto stage_addr = [&](int item) { return ring_addr + (item % NS) * L::kTileBytes; };
+    auto wait_item = [&](int item) {
+      return warp_wait(full + item % NS, (item / NS) & 1, abort_flag, a.status);
+    };
+    // S_x(j) = Q_x K(j)^T (issuing lane only).  A stage is released after its
+    // last use: dense K(j) and V(j) serve both units, so after unit b's.
+    auto issue_qk = [&](int x, int j) {
+      const int i = k_item(x, j);
+      const uint32_t kb = stage_addr(i), qb = q_addr + x * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // A = Q from TMEM, B = K tile
-          const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
-          umma_ts(tmem + (j & 1) * 128, tQ + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_qk,
-                  kk > 0);
-        }
-        umma_commit(s_full + (j & 1));
-        umma_commit(empty + st);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
+        umma_ss(tmem + x * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                idesc_qk, kk > 0);
       }
-      __syncwarp();
+      umma_commit(s_full + x);
+      if (kSparseMode || x == 1) umma_commit(empty + i % NS);
+    };
+    // O_x (+)= P_x(j) V(j), A = P from TMEM (issuing lane only)
+    auto issue_pv = [&](int x, int j) {
+      const int i = v_item(x, j);
+      const uint32_t vb = stage_addr(i);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        umma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8,
+                sdesc_sw128(vb + kk * 16 * 128, L::kSubBytes, 1024), idesc_pv,
+                (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (kSparseMode || x == 1) umma_commit(empty + i % NS);
+      if (j == nkv - 1) umma_commit(o_full + x);
+    };
+    // Sparse: wait for one operand, issue one product.  (Q and K/V rows are
+    // written by cp.async: a proxy fence after the waits makes them visible
+    // to the tensor core.)
+    auto qk = [&](int x, int j) -> bool {
+      if (!wait_item(k_item(x, j))) return false;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (elect_one()) issue_qk(x, j);
       return true;
     };
-    bool ok = warp_wait(q_full, 0, abort_flag, a.status) && issue_qk(0);
-    for (int j = 0; ok && j < nkv; ++j) {
-      // S(j+1) goes into the other buffer, whose P(j-1) was consumed by
-      // PV(j-1), issued earlier (MMAs of one thread execute in order).
-      if (j + 1 < nkv && !issue_qk(j + 1)) break;
-      if (!warp_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) break;
-      const int i = 2 * j + 1, st = i % NS;
-      if (!warp_wait(full + st, (i / NS) & 1, abort_flag, a.status)) break;
-      if (MODE != kDense) fence_proxy_async_smem();  // rows written by cp.async
+    auto pv = [&](int x, int j) -> bool {
+      if (!warp_wait(p_full + x, j & 1, abort_flag, a.status) || !wait_item(v_item(x, j)))
+        return false;
+      fence_proxy_async_smem();
       tc_fence_after();
-      const uint32_t vb = ring_addr + st * L::kTileBytes;
-      const uint32_t tP = tmem + (j & 1) * 128;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          umma_ts(tO, tP + kk * 8, sdesc_sw128(vb + kk * 16 * 128, L::kSubBytes, 1024), idesc_pv,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(o_done);
-        umma_commit(empty + st);
+      if (elect_one()) issue_pv(x, j);
+      return true;
+    };
+    bool ok = warp_wait(q_full, 0, abort_flag, a.status);
+    if (kSparseMode) {
+      ok = ok && qk(0, 0) && qk(1, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const bool last = j + 1 == nkv;
+        ok = pv(0, j) && (last || qk(0, j + 1)) && pv(1, j) && (last || qk(1, j + 1));
       }
-      __syncwarp();
+    } else {
+      ok = ok && wait_item(k_item(0, 0));
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+          issue_qk(0, 0);
+          issue_qk(1, 0);
+        }
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const bool more = j + 1 < nkv;
+        ok = wait_item(v_item(0, j)) && (!more || wait_item(k_item(0, j + 1)));
+        for (int x = 0; ok && x < 2; ++x) {
+          ok = warp_wait(p_full + x, j & 1, abort_flag, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(x, j);
+            if (more) issue_qk(x, j + 1);
+          }
+        }
+      }
     }
-    if (elect_one()) umma_commit(o_full);
-    __syncwarp();
-    drain_wait(o_full, 0);
+    drain_wait(o_full + 1, 0);
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // Warps 4x .. 4x+3 handle unit x; warp w reads TMEM lanes 32*(w%4) ...
+    // The 128 scores of a row are handled 64 at a time (the register budget
+    // of 16 warps): the max over both halves first, then the exponentials of
+    // columns 0-63 (kept in registers) and of columns 64-127 (loaded again).
+    // P of columns 0-63 goes over S columns 0-31, already read, and P of
+    // 64-127 over columns 32-63, read in the first half.
+    const int x = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;  // 0..127 == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + x * D + lane_off;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
-    {
-      // Q tile -> TMEM (the QK MMA's A operand, read from TMEM every tile
-      // instead of shared memory): row `row` holds its D bf16 values as D/2
-      // 32-bit columns, lower index in the low half.  Missing rows are zero.
-      int src = -1;
-      if (MODE == kDense) {
-        src = tile * BM + row;
-        if (src >= a.N) src = -1;
-      } else if (row < a.C) {
-        src = __ldg(a.perm + (static_cast<size_t>(bh) * a.G + tile) * a.C + row);
-        if (src >= a.N) {
-          atomicOr(a.status, DEV_BOUNDS);
-          src = -1;
-        }
-      }
-      const uint4* qrow = reinterpret_cast<const uint4*>(
-          a.q + (static_cast<size_t>(bh) * a.N + (src < 0 ? 0 : src)) * D);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {  // 32 columns (64 values) at a time
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 x = src >= 0 ? __ldg(qrow + c * 8 + i) : make_uint4(0, 0, 0, 0);
-          w[4 * i + 0] = x.x;
-          w[4 * i + 1] = x.y;
-          w[4 * i + 2] = x.z;
-          w[4 * i + 3] = x.w;
-        }
-        tmem_st32(tQ + lane_off + c * 32, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
     for (int j = 0; j < nkv; ++j) {
-      if (!warp_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      if (!warp_wait(s_full + x, j & 1, abort_flag, a.status)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + (j & 1) * 128 + lane_off;
-      float s[BN];
-      uint32_t* su = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
-      tmem_ld_wait();
       const int valid = kv_total - j * BN;
+      float s[64];
+      uint32_t* su = reinterpret_cast<uint32_t*>(s);
+      tmem_ld32(tS + 64, su);
+      tmem_ld32(tS + 96, su + 32);
+      tmem_ld_wait();
       if (valid < BN) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < 64; ++c)
+          if (c + 64 >= valid) s[c] = -INFINITY;
+      }
+      const float mx_hi = max64(s);
+      tmem_ld32(tS + 0, su);
+      tmem_ld32(tS + 32, su + 32);
+      tmem_ld_wait();
+      if (valid < 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
           if (c >= valid) s[c] = -INFINITY;
       }
-      // row max: four independent chains of 3-input max (short latency chain)
-      float mc0 = s[0], mc1 = s[1], mc2 = s[2], mc3 = s[3];
-#pragma unroll
-      for (int c = 4; c < BN; c += 8) {
-        mc0 = fmax3(mc0, s[c + 0], s[c + 1]);
-        mc1 = fmax3(mc1, s[c + 2], s[c + 3]);
-        mc2 = fmax3(mc2, s[c + 4 < BN ? c + 4 : 0], s[c + 5 < BN ? c + 5 : 0]);
-        mc3 = fmax3(mc3, s[c + 6 < BN ? c + 6 : 0], s[c + 7 < BN ? c + 7 : 0]);
-      }
-      const float mx = fmaxf(fmaxf(mc0, mc1), fmaxf(mc2, mc3));
-      const float m_new = mx * sl2;
+      const float m_new = fmaxf(max64(s), mx_hi) * sl2;
       // Lazy rescaling: a row's reference max only moves when the tile max
       // exceeds it by more than the threshold.  TMEM loads/stores are
       // warp-collective, so the whole warp enters the rescale when any of its
-      // rows needs it (f = 1 for the others).  O may still be accumulating
-      // PV(j-1): wait for it first (PV(j) cannot start before this P(j)).
+      // rows needs it (f = 1 for the others).  PV_x(j-1) has completed: it
+      // was issued before QK_x(j), whose completion this warp has seen.
       const bool need = (j > 0) && (m_new > m_run + kRescaleThreshold);
       if (j == 0) m_run = m_new;
       if (__any_sync(0xffffffffu, need)) {
-        if (!warp_wait(o_done, (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
-        tc_fence_after();
         const float f = need ? ex2(m_run - m_new) : 1.f;
         l_f32 *= f;
         l_b16 *= f;
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
           uint32_t o[16];
-          tmem_ld16(tO + lane_off + c * 16, o);
+          tmem_ld16(tO + c * 16, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(f * __uint_as_float(o[i]));
-          tmem_st16(tO + lane_off + c * 16, o);
+          tmem_st16(tO + c * 16, o);
         }
         if (need) m_run = m_new;
       }
@@ -382,45 +466,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_run, -m_run);
       uint64_t accf[4] = {0ull, 0ull, 0ull, 0ull}, accb[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t pk[16];
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1) {
+          tmem_ld32(tS + 64, su);
+          tmem_ld32(tS + 96, su + 32);
+          tmem_ld_wait();
+          if (valid < BN) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), c2, nm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          pk[i] = pack_bf16(p0, p1);
-          accf[i & 3] = f2_add(accf[i & 3], f2_pack(p0, p1));
-          accb[i & 3] = f2_add(accb[i & 3], f2_pack(__uint_as_float(pk[i] << 16),
-                                                    __uint_as_float(pk[i] & 0xFFFF0000u)));
+            for (int c = 0; c < 64; ++c)
+              if (c + 64 >= valid) s[c] = -INFINITY;
+          }
         }
-        tmem_st16(tS + c * 16, pk);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), c2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[i] = pack_bf16(p0, p1);
+            accf[i & 3] = f2_add(accf[i & 3], f2_pack(p0, p1));
+            accb[i & 3] = f2_add(accb[i & 3], f2_pack(__uint_as_float(pk[i] << 16),
+                                                      __uint_as_float(pk[i] & 0xFFFF0000u)));
+          }
+          tmem_st16(tS + h * 32 + c * 16, pk);
+        }
       }
       l_f32 += sum8(accf);
       l_b16 += sum8(accb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + (j & 1));
+      if (lane == 0) mbar_arrive(p_full + x);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && warp_wait(o_full, 0, abort_flag, a.status)) {
+    if (ok && warp_wait(o_full + x, 0, abort_flag, a.status)) {
       tc_fence_after();
       const float inv_l = 1.f / l_b16;
+      const int unit = 2 * pair + x;
       int token;
-      if (MODE == kDense) {
-        token = tile * BM + row;
+      if (!kSparseMode) {
+        token = unit * BM + row;
         if (token >= a.N) token = -1;
       } else {
-        token = (row < a.C) ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + tile) * a.C + row)
-                            : -1;
+        token = (row < a.C && (x == 0 || has_b))
+                    ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + unit) * a.C + row)
+                    : -1;
         if (token >= a.N) token = -1;
       }
       const size_t row_off = (static_cast<size_t>(bh) * a.N + (token < 0 ? 0 : token)) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
         if (token >= 0) {
           float v[32];
@@ -431,10 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 w = __ldg(src + q4);
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+              const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                float2 f2 = __bfloat1622float2(h[e]);
+                float2 f2 = __bfloat1622float2(hh[e]);
                 const int i0 = q4 * 8 + 2 * e;
                 if (MODE == kSparseAdd) {
                   v[i0] += f2.x;
@@ -458,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (MODE == kDense && a.lse != nullptr && token >= 0)
+      if (!kSparseMode && a.lse != nullptr && token >= 0)
         a.lse[static_cast<size_t>(bh) * a.N + token] =
             (m_run + __log2f(l_f32)) * 0.69314718055994531f;
     }
@@ -477,8 +576,8 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   const int smem = AttnLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int gx = (MODE == kDense) ? (a.N + BM - 1) / BM : a.G;
-  kern<<<dim3(gx, BH), kThreads, smem, stream>>>(*tq, *tk, *tv, a);
+  const int units = (MODE == kDense) ? (a.N + BM - 1) / BM : a.G;
+  kern<<<dim3((units + 1) / 2, BH), kThreads, smem, stream>>>(*tq, *tk, *tv, a);
   return cudaGetLastError();
 }
 

@@ -123,6 +123,14 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 
+// As cp_async16, but when !valid nothing is read and the 16 bytes are zeroed
+// (src must still be a mapped address).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
 // Arrive on the mbarrier once every cp.async this thread issued so far has
 // landed (the barrier's expected count includes this thread).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
