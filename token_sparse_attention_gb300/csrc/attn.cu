@@ -32,7 +32,9 @@
 // in-order MMA stream; and a commit signals completion of every earlier MMA,
 // so a softmax warp that sees S_x(j) complete knows PV_x(j-1) is done too.
 // Online softmax in base 2 with lazy rescaling (O is rescaled only when a
-// row's running max grows by more than 8, so P <= 256).
+// row's running max grows by more than 16, so P <= 2^16; P is bf16 (relative
+// rounding whatever its size) and O and the row sums are fp32, whose range
+// that bound leaves untouched: 2^16 * N * |v| stays far below 2^127).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -46,7 +48,7 @@ constexpr int kProducers = 7;
 constexpr int kFirstProducer = kSoftmaxWarps;
 constexpr int kMmaWarp = kFirstProducer + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 16.0f;
 
 template <int D>
 struct AttnLayout {
@@ -267,6 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
         return true;
       };
+      // Both groups' index rows (K entries each) are read once, from HBM:
+      // pull them into L2 now so that the per-tile index loads below hit L2.
+      for (int x = 0; x < 2; ++x) {
+        const char* idx_g = reinterpret_cast<const char*>(
+            a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K);
+        for (int off = tid * 128; off < a.K * 4; off += kPT * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(idx_g + off));
+      }
       // rows of tiles j (V_x(j)), j+1 (K_x(j+1)) and j+2 (being fetched)
       int r0[2][kPer], r1[2][kPer], r2[2][kPer];
       load_rows(0, 0, r0[0]);
@@ -279,12 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < nkv; ++j) {
         if (a.fault && j >= 1) break;  // test-only: starve the MMA warp
         const bool more = j + 1 < nkv;
+        for (int x = 0; ok && x < 2; ++x)
+          ok = copy_tile(v_item(x, j), a.v, r0[x]) && (!more || copy_tile(k_item(x, j + 1), a.k, r1[x]));
+        // indices of tile j+2, after this step's copies: their load latency
+        // then delays nothing already due
         if (j + 2 < nkv) {
           load_rows(0, j + 2, r2[0]);
           load_rows(1, j + 2, r2[1]);
         }
-        for (int x = 0; ok && x < 2; ++x)
-          ok = copy_tile(v_item(x, j), a.v, r0[x]) && (!more || copy_tile(k_item(x, j + 1), a.k, r1[x]));
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           r0[0][k] = r1[0][k];
@@ -304,15 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     //
     // The first mbarrier operation after a batch stalls until the tensor core
     // has taken nearly the whole batch (it buffers only one or two MMAs), so
-    // a wait between batches is time the tensor core may sit idle.
-    //  Dense: per step the issuer waits for the step's K/V tiles at once (TMA
-    //    loads them well ahead), then issues PV_x(j) and QK_x(j+1) of a unit
-    //    as one batch, so that only the waits for P_a(j) and P_b(j) fall
-    //    between batches.
-    //  Sparse: each product waits only for its own operand and is issued on
-    //    its own: the gathered rows arrive just in time in the shallower ring
-    //    (four tiles per step), and tying PV_x(j) to the later K_x(j+1)
-    //    gather would hold it back.
+    // a wait between batches is time the tensor core may sit idle.  PV_x(j)
+    // and QK_x(j+1) of a unit are therefore issued as one batch, after the
+    // waits for its operands (V_x(j) and K_x(j+1), loaded well ahead) and for
+    // P_x(j).
     constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
     const uint32_t ring_addr = smem_u32(ring);
@@ -348,51 +355,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kSparseMode || x == 1) umma_commit(empty + i % NS);
       if (j == nkv - 1) umma_commit(o_full + x);
     };
-    // Sparse: wait for one operand, issue one product.  (Q and K/V rows are
-    // written by cp.async: a proxy fence after the waits makes them visible
-    // to the tensor core.)
-    auto qk = [&](int x, int j) -> bool {
-      if (!wait_item(k_item(x, j))) return false;
-      fence_proxy_async_smem();
+    bool ok = warp_wait(q_full, 0, abort_flag, a.status) && wait_item(k_item(0, 0)) &&
+              wait_item(k_item(1, 0));
+    if (ok) {
+      if (kSparseMode) fence_proxy_async_smem();
       tc_fence_after();
-      if (elect_one()) issue_qk(x, j);
-      return true;
-    };
-    auto pv = [&](int x, int j) -> bool {
-      if (!warp_wait(p_full + x, j & 1, abort_flag, a.status) || !wait_item(v_item(x, j)))
-        return false;
-      fence_proxy_async_smem();
-      tc_fence_after();
-      if (elect_one()) issue_pv(x, j);
-      return true;
-    };
-    bool ok = warp_wait(q_full, 0, abort_flag, a.status);
-    if (kSparseMode) {
-      ok = ok && qk(0, 0) && qk(1, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const bool last = j + 1 == nkv;
-        ok = pv(0, j) && (last || qk(0, j + 1)) && pv(1, j) && (last || qk(1, j + 1));
+      if (elect_one()) {
+        issue_qk(0, 0);
+        issue_qk(1, 0);
       }
-    } else {
-      ok = ok && wait_item(k_item(0, 0));
-      if (ok) {
+    }
+    for (int j = 0; ok && j < nkv; ++j) {
+      const bool more = j + 1 < nkv;
+      for (int x = 0; ok && x < 2; ++x) {
+        // Probe the batch's barriers together (their latencies overlap);
+        // only if one is not complete yet wait for each in turn.
+        const int iv = v_item(x, j), ik = more ? k_item(x, j + 1) : iv;
+        const bool ready = mbar_try_wait(full + iv % NS, (iv / NS) & 1) &
+                           mbar_try_wait(full + ik % NS, (ik / NS) & 1) &
+                           mbar_try_wait(p_full + x, j & 1);
+        if (!__all_sync(0xffffffffu, ready))
+          ok = wait_item(iv) && wait_item(ik) && warp_wait(p_full + x, j & 1, abort_flag, a.status);
+        if (!ok) break;
+        if (kSparseMode) fence_proxy_async_smem();
         tc_fence_after();
         if (elect_one()) {
-          issue_qk(0, 0);
-          issue_qk(1, 0);
-        }
-      }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const bool more = j + 1 < nkv;
-        ok = wait_item(v_item(0, j)) && (!more || wait_item(k_item(0, j + 1)));
-        for (int x = 0; ok && x < 2; ++x) {
-          ok = warp_wait(p_full + x, j & 1, abort_flag, a.status);
-          if (!ok) break;
-          tc_fence_after();
-          if (elect_one()) {
-            issue_pv(x, j);
-            if (more) issue_qk(x, j + 1);
-          }
+          issue_pv(x, j);
+          if (more) issue_qk(x, j + 1);
         }
       }
     }
