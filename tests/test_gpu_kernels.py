@@ -96,6 +96,41 @@ def test_sparse_attention(B, H, N, D, C, K):
             P.assert_close(out[b, h], want, f"sparse b{b} h{h}")
 
 
+@pytest.mark.parametrize("D,C", [(64, 64), (128, 128)])
+def test_long_kv_many_ring_turns(D, C):
+    """Many more K/V tiles than ring stages, so that the K/V ring and the
+    kernel's batch-completion barriers wrap around many times (a phase-parity
+    mistake there shows up as a timed-out wait in the status word): dense and
+    sparse, checked on sampled rows and groups."""
+    N, K = 6000, 3000
+    q, k, v = P.random_qkv(1, 2, N, D, seed=D + 5)
+    qd, kd, vd = _dev(q, k, v)
+    p = mcs.params(1, 2, N, D, C, K)
+    scale = orc.default_scale(D)
+    rng = np.random.default_rng(D)
+    out = torch.empty_like(qd)
+    lse = torch.empty(1, 2, N, dtype=torch.float32, device="cuda")
+    mcs.mcs_dense_attn(p, qd, kd, vd, out, lse)
+    assert mcs.mcs_device_status() == 0
+    rows = np.sort(rng.choice(N, 48, replace=False))
+    for h in range(2):
+        O, L = orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale, rows=rows)
+        P.assert_close(out[0, h][rows], O, f"dense rows h{h}")
+        assert np.max(np.abs(P.f64(lse[0, h][rows]) - L)) <= P.LSE_ABS
+    G = -(-N // C)
+    perm = np.stack([P.random_groups(N, C, 40 + h) for h in range(2)])[None]
+    idx = np.stack([P.random_idx(N, G, K, 50 + h) for h in range(2)])[None]
+    out2 = torch.full_like(qd, float("nan"))
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), None, out2)
+    assert mcs.mcs_device_status() == 0
+    for h in range(2):
+        qh, kh, vh = P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h])
+        for g in [0, G - 1] + list(rng.choice(np.arange(1, G - 1), 3, replace=False)):
+            m = orc.group_members(perm[0, h], g, C)
+            want = orc.sparse_attention_group(qh, kh, vh, m, idx[0, h, g], scale)
+            P.assert_close(out2[0, h][torch.from_numpy(m).cuda()], want, f"sparse h{h} g{g}")
+
+
 def test_sparse_residual_add_and_record():
     B, H, N, D, C, K = 1, 2, 700, 128, 128, 150
     q, k, v, perm, idx = _sparse_case(B, H, N, D, C, K, seed=5)

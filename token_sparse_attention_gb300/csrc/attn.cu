@@ -49,6 +49,14 @@ constexpr int kFirstProducer = kSoftmaxWarps;
 constexpr int kMmaWarp = kFirstProducer + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kRescaleThreshold = 16.0f;
+// Batch-completion barriers, used round robin.  A waiter on batch n reads the
+// phase parity of done[n % kDone]; that is unambiguous as long as batch
+// n + kDone cannot have completed yet.  The producers lag furthest: before
+// loading ring item i they wait for the last batch reading item i - NS, and
+// the batches that can complete meanwhile are those whose items are all
+// below i: at most NS - 1 later (dense, 2 items per step) or NS / 2 later
+// (sparse, 4 items per step).  16 covers both rings (NS <= 12).
+constexpr int kDone = 16;
 
 template <int D>
 struct AttnLayout {
@@ -59,7 +67,7 @@ struct AttnLayout {
   static constexpr int kQ = 0;                         // Q_a, Q_b
   static constexpr int kRing = 2 * kTileBytes;
   static constexpr int kBars = kRing + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kNumBars = kStages + kDone + 3;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
@@ -123,11 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem + L::kRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* full = bars;              // [NS] stage loaded
-  uint64_t* empty = bars + NS;        // [NS] stage consumed by its last MMA
-  uint64_t* q_full = bars + 2 * NS;   // Q_a and Q_b loaded
-  uint64_t* s_full = q_full + 1;      // [2] S_x(j) computed
-  uint64_t* p_full = q_full + 3;      // [2] P_x(j) written (4 warp arrivals)
-  uint64_t* o_full = q_full + 5;      // [2] every PV of unit x complete
+  uint64_t* done = bars + NS;         // [kDone] MMA batch n complete: done[n % kDone]
+  uint64_t* q_full = done + kDone;    // Q_a and Q_b loaded
+  uint64_t* p_full = q_full + 1;      // [2] P_x(j) written (4 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -149,18 +155,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     return kSparseMode ? (j == 0 ? x : 4 * j - 1 + 2 * x) : 2 * j;
   };
   auto v_item = [&](int x, int j) { return kSparseMode ? 4 * j + 2 + 2 * x : 2 * j + 1; };
-
+  // MMA batches, in issue order: batch 0 = QK_a(0) QK_b(0); batch 2j+x+1 =
+  // PV_x(j) QK_x(j+1).  Each batch ends with ONE commit, on done[n % kDone]:
+  // that commit signals completion of every earlier MMA too, so it serves
+  // the softmax (S_x ready), the epilogue (O_x final) and the producers
+  // (stages free).
+  static_assert(kDone >= NS, "batch barriers must outnumber the producer lag");
+  auto wait_batch = [&](int n) {
+    return warp_wait(done + n % kDone, (n / kDone) & 1, abort_flag, a.status);
+  };
+  // last batch that reads ring item i (its stage is free once it is done)
+  auto release_batch = [&](int i) {
+    return kSparseMode ? i >> 1 : ((i & 1) ? i + 1 : i);
+  };
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NS; ++s)
       mbar_init(full + s, kSparseMode ? 32 * kProducers : 1);  // sparse: every producer thread
-      mbar_init(empty + s, 1);
-    }
+    for (int n = 0; n < kDone; ++n) mbar_init(done + n, 1);
     mbar_init(q_full, kSparseMode ? 32 * kProducers : 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(s_full + x, 1);
-      mbar_init(p_full + x, 4);
-      mbar_init(o_full + x, 1);
-    }
+    for (int x = 0; x < 2; ++x) mbar_init(p_full + x, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -193,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2 * nkv; ++i) {
           if (a.fault && i >= 2) break;  // test-only: starve the MMA warp
           const int st = i % NS;
-          if (i >= NS && !warp_wait(empty + st, ((i / NS) - 1) & 1, abort_flag, a.status)) break;
+          if (i >= NS && !wait_batch(release_batch(i - NS))) break;
           if (elect_one()) {
             mbar_expect_tx(full + st, L::kTileBytes);
             const CUtensorMap* tm = (i & 1) ? &tv : &tk;
@@ -254,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Copy the rows of one K or V tile into the stage of ring item `it`.
       auto copy_tile = [&](int it, const __nv_bfloat16* src, const int* rows) -> bool {
         const int st = it % NS;
-        if (it >= NS && !warp_wait(empty + st, ((it / NS) - 1) & 1, abort_flag, a.status))
-          return false;
+        if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
         uint8_t* stage = ring + st * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
@@ -328,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_item = [&](int item) {
       return warp_wait(full + item % NS, (item / NS) & 1, abort_flag, a.status);
     };
-    // S_x(j) = Q_x K(j)^T (issuing lane only).  A stage is released after its
-    // last use: dense K(j) and V(j) serve both units, so after unit b's.
+    // S_x(j) = Q_x K(j)^T (issuing lane only)
     auto issue_qk = [&](int x, int j) {
       const int i = k_item(x, j);
       const uint32_t kb = stage_addr(i), qb = q_addr + x * L::kTileBytes;
@@ -339,8 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_ss(tmem + x * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                 idesc_qk, kk > 0);
       }
-      umma_commit(s_full + x);
-      if (kSparseMode || x == 1) umma_commit(empty + i % NS);
     };
     // O_x (+)= P_x(j) V(j), A = P from TMEM (issuing lane only)
     auto issue_pv = [&](int x, int j) {
@@ -352,8 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sdesc_sw128(vb + kk * 16 * 128, L::kSubBytes, 1024), idesc_pv,
                 (j > 0 || kk > 0) ? 1u : 0u);
       }
-      if (kSparseMode || x == 1) umma_commit(empty + i % NS);
-      if (j == nkv - 1) umma_commit(o_full + x);
     };
     bool ok = warp_wait(q_full, 0, abort_flag, a.status) && wait_item(k_item(0, 0)) &&
               wait_item(k_item(1, 0));
@@ -363,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) {
         issue_qk(0, 0);
         issue_qk(1, 0);
+        umma_commit(done);
       }
     }
     for (int j = 0; ok && j < nkv; ++j) {
@@ -380,12 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kSparseMode) fence_proxy_async_smem();
         tc_fence_after();
         if (elect_one()) {
+          const int n = 2 * j + x + 1;
           issue_pv(x, j);
           if (more) issue_qk(x, j + 1);
+          umma_commit(done + n % kDone);
         }
       }
     }
-    drain_wait(o_full + 1, 0);
+    const int n_last = 2 * nkv;
+    drain_wait(done + n_last % kDone, (n_last / kDone) & 1);
   } else {
     // ------------------------------------------------------------ softmax
     // Warps 4x .. 4x+3 handle unit x; warp w reads TMEM lanes 32*(w%4) ...
@@ -403,7 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!warp_wait(s_full + x, j & 1, abort_flag, a.status)) { ok = false; break; }
+      if (!wait_batch(j == 0 ? 0 : 2 * j + x - 1)) {  // S_x(j) written
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const int valid = kv_total - j * BN;
       float s[64];
@@ -490,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(p_full + x);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && warp_wait(o_full + x, 0, abort_flag, a.status)) {
+    if (ok && wait_batch(2 * nkv + x - 1)) {  // the last PV_x complete
       tc_fence_after();
       const float inv_l = 1.f / l_b16;
       const int unit = 2 * pair + x;

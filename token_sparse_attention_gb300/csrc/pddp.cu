@@ -233,13 +233,16 @@ __global__ void __launch_bounds__(kMomThreads, 2)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, D, true, true);
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(ready + st, (j >> 1) & 1, abort_flag, status)) break;
-        tc_fence_after();
-        const uint32_t base = smem_u32(smem + st * L::kStage);
+    // whole warp in the loop, one elected lane issues (a lane-0-only branch
+    // issues MMAs much more slowly)
+    constexpr uint32_t idesc = idesc_bf16(128, D, true, true);
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      const bool ok = mbar_wait(ready + st, (j >> 1) & 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t base = smem_u32(smem + st * L::kStage);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t d = sdesc_sw128(base + kk * 16 * 128, L::kSubBytes, 1024);
@@ -247,11 +250,12 @@ __global__ void __launch_bounds__(kMomThreads, 2)
         }
         umma_commit(empty + st);
       }
-      umma_commit(done);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(done, 0))
-        if (clock64() - t0 > kWaitLimitCycles) break;
     }
+    if (elect_one()) umma_commit(done);
+    __syncwarp();
+    const long long t0 = clock64();
+    while (!mbar_try_wait(done, 0))
+      if (clock64() - t0 > kWaitLimitCycles) break;
   } else {
     // ------------------------------------------------------------ row sums, tails, epilogue
     const int t = threadIdx.x;  // 0..127

@@ -13,7 +13,7 @@
 // in registers: no cross-thread reduction and no running max (lse is known).
 //   warps 0-3  exp + sum, one KV row per thread, write mass[g, j]
 //   warp 4     producer: gather4 of the group's Q rows, TMA tiles of K
-//   warp 5     TMEM allocation and the MMA-issuing thread
+//   warp 5     TMEM allocation and MMA issue (one elected lane)
 // Two K stages and two TMEM score buffers let the MMA of tile j+1 run while
 // tile j is exponentiated.
 //
@@ -132,33 +132,36 @@ __global__ void __launch_bounds__(kMassThreads, 2)
         tma_gather4(sq + s * L::kQSub + r4 * 4 * 128, &tq, s * 64, r[0], r[1], r[2], r[3], q_full);
     }
     if (bad) atomicOr(a.status, DEV_BOUNDS);
-    if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(k_empty + st, ((j >> 1) - 1) & 1, abort_flag, a.status)) break;
+    // K tiles: the whole warp runs the loop, an elected lane issues (a
+    // lane-0-only branch issues TMA and MMA instructions much more slowly)
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (j >= 2 && !warp_wait_m(k_empty + st, ((j >> 1) - 1) & 1, abort_flag, a.status)) break;
+      if (elect_one()) {
         mbar_expect_tx(k_full + st, L::kKStage);
         for (int s = 0; s < L::kSub; ++s)
           tma_load_3d(sk + st * L::kKStage + s * L::kKSub, &tk, s * 64, j * 128, bh, k_full + st);
-        ++issued;
       }
-      if (*abort_flag) {
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-          drain_wait_m(k_full + (j & 1), (j >> 1) & 1);
-      }
+      ++issued;
+    }
+    if (*abort_flag) {
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+        drain_wait_m(k_full + (j & 1), (j >> 1) & 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, CQ, false, false);
-      const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk);
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.status);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(k_full + st, (j >> 1) & 1, abort_flag, a.status)) break;
-        if (j >= 2 && !mbar_wait(s_empty + st, ((j >> 1) - 1) & 1, abort_flag, a.status)) break;
-        tc_fence_after();
-        const uint32_t kb = k_addr + st * L::kKStage;
+    // whole warp in the loop, one elected lane issues each tile's MMAs
+    constexpr uint32_t idesc = idesc_bf16(128, CQ, false, false);
+    const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk);
+    bool ok = warp_wait_m(q_full, 0, abort_flag, a.status);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int st = j & 1;
+      if (!warp_wait_m(k_full + st, (j >> 1) & 1, abort_flag, a.status)) break;
+      if (j >= 2 && !warp_wait_m(s_empty + st, ((j >> 1) - 1) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t kb = k_addr + st * L::kKStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * L::kKSub + (kk & 3) * 32;
@@ -169,9 +172,10 @@ __global__ void __launch_bounds__(kMassThreads, 2)
         umma_commit(s_full + st);
         umma_commit(k_empty + st);
       }
-      umma_commit(done);
-      drain_wait_m(done, 0);
     }
+    if (elect_one()) umma_commit(done);
+    __syncwarp();
+    drain_wait_m(done, 0);
   } else {
     // ------------------------------------------------------------ exp + sum
     const int t = threadIdx.x;  // 0..127: KV row within the tile == TMEM lane
