@@ -131,6 +131,42 @@ def test_long_kv_many_ring_turns(D, C):
             P.assert_close(out2[0, h][torch.from_numpy(m).cuda()], want, f"sparse h{h} g{g}")
 
 
+def test_many_unit_pairs_per_cta():
+    """More query-unit pairs than SMs, so that every CTA of the persistent
+    kernels processes several pairs one after another (Q buffers, TMEM
+    accumulators and barrier phases reused across pairs), dense and sparse
+    with residual; checked on sampled rows and groups."""
+    B, H, N, D, C, K = 1, 2, 40000, 128, 128, 300  # 157 pairs per head
+    q, k, v = P.random_qkv(B, H, N, D, seed=77)
+    qd, kd, vd = _dev(q, k, v)
+    p = mcs.params(B, H, N, D, C, K)
+    scale = orc.default_scale(D)
+    rng = np.random.default_rng(78)
+    out = torch.empty_like(qd)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    mcs.mcs_dense_attn(p, qd, kd, vd, out, lse)
+    assert mcs.mcs_device_status() == 0
+    rows = np.sort(rng.choice(N, 40, replace=False))
+    for h in range(H):
+        O, L = orc.dense_attention(P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h]), scale, rows=rows)
+        P.assert_close(out[0, h][rows], O, f"dense rows h{h}")
+        assert np.max(np.abs(P.f64(lse[0, h][rows]) - L)) <= P.LSE_ABS
+    G = -(-N // C)
+    perm = np.stack([P.random_groups(N, C, 80 + h) for h in range(H)])[None]
+    idx = np.stack([P.random_idx(N, G, K, 90 + h) for h in range(H)])[None]
+    r = (0.05 * torch.randn(B, H, N, D, generator=torch.Generator().manual_seed(79),
+                            dtype=torch.float64)).to(torch.bfloat16)
+    out2 = torch.full_like(qd, float("nan"))
+    mcs.mcs_sparse_attn(p, qd, kd, vd, _i32(perm), _i32(idx), r.cuda(), out2)
+    assert mcs.mcs_device_status() == 0
+    for h in range(H):
+        qh, kh, vh = P.f64(q[0, h]), P.f64(k[0, h]), P.f64(v[0, h])
+        for g in [0, 1, G - 1] + list(rng.choice(np.arange(2, G - 1), 5, replace=False)):
+            m = orc.group_members(perm[0, h], g, C)
+            want = orc.sparse_attention_group(qh, kh, vh, m, idx[0, h, g], scale) + P.f64(r[0, h])[m]
+            P.assert_close(out2[0, h][torch.from_numpy(m).cuda()], want, f"sparse h{h} g{g}")
+
+
 def test_sparse_residual_add_and_record():
     B, H, N, D, C, K = 1, 2, 700, 128, 128, 150
     q, k, v, perm, idx = _sparse_case(B, H, N, D, C, K, seed=5)
