@@ -51,7 +51,7 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 TRAFFIC = {
     # ncu dram bytes (read + write) of the sparse reuse launch of the 4-head
     # large workload, times 10 for the 40-head launch (heads are independent)
-    "attn.cu": {"sha": "fa774a25284c", "bytes_per_launch": 10 * (625954048 + 68949760)},
+    "attn.cu": {"sha": "96176a4dc22a", "bytes_per_launch": 10 * (664201216 + 69140480)},
 }
 
 
