@@ -66,6 +66,21 @@ def _peaks():
             "fallback"
 
 
+def reduce_max_over_ranks(vals, dist, device):
+    """Max of each value over all ranks (every rank gets the result); the
+    job's time is that of its slowest replica."""
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(world: int, flops_per_replica: float, ms: float) -> float:
+    """Whole-job throughput of `world` independent replicas that each do
+    flops_per_replica in `ms` (the max over ranks): weak scaling."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 def _src_sha(name: str) -> str:
     with open(os.path.join(ROOT, "token_sparse_attention_gb300", "csrc", name), "rb") as f:
         return hashlib.sha1(f.read()).hexdigest()[:12]
@@ -328,17 +343,14 @@ def run_gpu(args, w, K, rank, world, dist):
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
 
     # ---- max over ranks
-    vals = torch.tensor([total_ms, stage_ms["reuse"], stage_ms["dense"],
-                         e2e["ms"] if e2e else 0.0], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, t_sparse, t_dense, e2e_ms = vals.tolist()
+    total_ms, t_sparse, t_dense, e2e_ms = reduce_max_over_ranks(
+        [total_ms, stage_ms["reuse"], stage_ms["dense"], e2e["ms"] if e2e else 0.0], dist, dev)
     if rank != 0:
         return
 
     flops_sparse = 4.0 * BH * w.N * K * w.D
     flops_dense = 4.0 * BH * w.N * w.N * w.D
-    value = world * flops_sparse / (t_sparse * 1e-3) / 1e12
+    value = job_tflops(world, flops_sparse, t_sparse)
     speedup = t_dense / t_sparse
     peaks, peak_kind = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -392,7 +404,7 @@ def run_gpu(args, w, K, rank, world, dist):
         },
         "speedup_vs_dense": speedup,
         "efficiency_vs_ideal": speedup * args.density,
-        "dense_equivalent_tflops": world * flops_dense / (t_sparse * 1e-3) / 1e12,
+        "dense_equivalent_tflops": job_tflops(world, flops_dense, t_sparse),
         "stage_ms": stage_ms,
         "kernels": kernels,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -400,7 +412,7 @@ def run_gpu(args, w, K, rank, world, dist):
                      "kernel": "token-sparse attention (reuse step)",
                      "peak_source": f"bf16_tflops_sustained ({peak_kind})"},
         "cpu_baseline": cpu,
-        "e2e": ({"value": world * flops_sparse / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": ({"value": job_tflops(world, flops_sparse, e2e_ms), "unit": "TFLOP/s",
                  "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                  "ms_per_step": e2e_ms,
                  "pipelining": "step i+1's host->device copies overlap step i's kernel"}
