@@ -242,9 +242,6 @@ def run_gpu(args, w, K, rank, world, dist):
     retained = torch.empty(w.B, w.H, G, dtype=torch.float32, device=dev)
     ws_bytes = mcs.mcs_anchor_workspace(p)
     ws = mcs.empty_workspace(ws_bytes, dev)
-    per_head = -(-(G * w.N * 4) // 256) * 256
-    chunk = max(1, min(BH, ws_bytes // per_head))
-    mass = ws[: chunk * G * w.N * 4].view(torch.float32).view(chunk, G, w.N)
     stream = torch.cuda.current_stream()
     stages = ["pddp", "dense", "select", "record", "reuse"]
 
@@ -254,11 +251,7 @@ def run_gpu(args, w, K, rank, world, dist):
         ev[1].record(stream)
         mcs.mcs_dense_attn(p, q0, k0, v0, dense, lse)
         ev[2].record(stream)
-        for h0 in range(0, BH, chunk):
-            hc = min(chunk, BH - h0)
-            mcs.mcs_group_mass(p, q0, k0, lse, perm, h0, hc, mass[:hc])
-            mcs.mcs_topk(p, mass[:hc], idx.view(BH, G, K)[h0:h0 + hc],
-                         retained.view(BH, G)[h0:h0 + hc])
+        mcs.mcs_select(p, q0, k0, lse, perm, idx, ws, retained)
         ev[3].record(stream)
         mcs.mcs_sparse_attn_record(p, q0, k0, v0, perm, idx, dense, res)
         ev[4].record(stream)
@@ -373,6 +366,10 @@ def run_gpu(args, w, K, rank, world, dist):
         "pddp": {"ms": stage_ms["pddp"]},
     }
     depths = max(0, math.ceil(math.log2(G))) if G > 1 else 0
+    # mcs_select passes the heads through the workspace in chunks; each chunk
+    # is one group-mass and one top-K launch
+    rup = lambda x: -(-x // 256) * 256  # noqa: E731
+    chunk = max(1, min(BH, ws_bytes // (rup(G * w.N * 4) + rup(G * 2048 * 4))))
     n_chunks = -(-BH // chunk)
     launches = (2 + 4 * depths) + 1 + 2 * n_chunks + 1 + 1
     cores = len(os.sched_getaffinity(0))

@@ -129,6 +129,26 @@ mcs_status mcs_topk(const mcs_params* p, const float* mass, int rows, int32_t* i
                     float* retained, cudaStream_t stream);
 
 /*
+ * a3 + a4 as the anchor step runs them (ai.info AI summary, "Methodology in
+ * Plain English": the second selector pass fuses group aggregation with
+ * top-K).  From q, k, the dense pass's lse and the groups perm, writes idx
+ * [B,H,G,K] (each group's K KV indices of largest mass, ties to the lower
+ * index, ascending) and, when `retained` is not NULL, retained [B,H,G] (their
+ * mass sums): the same results as mcs_group_mass followed by mcs_topk.  Each
+ * group's masses are histogrammed by their top 12 bits as they are computed,
+ * so the top-K finds the K-th mass's bucket without reading them and reads
+ * them once; a group whose bucket holds more than 4096 masses (mass ties en
+ * masse) is selected in four reads instead.
+ * ws: device workspace through which the masses and histograms pass, heads
+ * in chunks: mcs_anchor_workspace(p) bytes process every head at once (up to
+ * 4 GiB); at least G*(N+2048)*4 bytes (each part rounded up to 256) are
+ * needed.  Requires K <= N.
+ */
+mcs_status mcs_select(const mcs_params* p, const void* q, const void* k, const float* lse,
+                      const int32_t* perm, int32_t* idx, float* retained, void* ws,
+                      size_t ws_bytes, cudaStream_t stream);
+
+/*
  * a5 + a6 -- Token-sparse attention (wispaper.ai, "Token-level selection
  * needs tile-aligned query groups"; "Residual correction recovers the
  * discarded tail").  For every group g of every head: the group's queries
@@ -155,11 +175,12 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
  * The whole anchor step (wispaper.ai, "Reused exact selection beats
  * recomputed mean pooling"; "Residual correction recovers the discarded
  * tail"): a1 grouping -> perm; a2 dense attention -> dense_out (the step's
- * output) and lse; a3 + a4 exact selection -> idx (and retained mass
- * [B,H,G], nullable); a5 anchor form -> residual.
+ * output) and lse; a3 + a4 exact selection (as mcs_select) -> idx (and
+ * retained mass [B,H,G], nullable); a5 anchor form -> residual.
  * ws: device workspace of at least mcs_anchor_workspace(p) bytes; a smaller
- * one (but at least one head's group masses, G*N*4 bytes, and the grouping
- * workspace) processes fewer heads per selection pass.
+ * one (but at least one head's group masses and histograms, G*(N+2048)*4
+ * bytes rounded up to 256-byte multiples, and the grouping workspace)
+ * processes fewer heads per selection pass.
  */
 mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, const void* v,
                              int32_t* perm, int32_t* idx, void* dense_out, float* lse,

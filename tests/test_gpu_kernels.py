@@ -374,6 +374,73 @@ def test_anchor_select_on_clusters_matches_oracle():
         assert np.max(np.abs(r + a["sparse"] - P.f64(dense[0, h]))) <= P.MAX_ABS
 
 
+def _anchor(p, q, k, v):
+    """Run mcs_anchor_select; returns (perm, idx, lse, retained)."""
+    BH = p.B * p.H
+    perm = torch.empty(p.B, p.H, p.G * p.C, dtype=torch.int32, device="cuda")
+    idx = torch.empty(p.B, p.H, p.G, p.K, dtype=torch.int32, device="cuda")
+    dense = torch.empty_like(q)
+    res = torch.empty_like(q)
+    lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device="cuda")
+    ret = torch.empty(p.B, p.H, p.G, dtype=torch.float32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+    mcs.mcs_anchor_select(p, q, k, v, perm, idx, dense, lse, res, ws, retained=ret)
+    assert mcs.mcs_device_status() == 0
+    assert BH == perm.shape[0] * perm.shape[1]
+    return perm, idx, lse, ret
+
+
+def _two_pass_select(p, q, k, lse, perm):
+    """The same selection through mcs_group_mass + mcs_topk (no histogram)."""
+    BH = p.B * p.H
+    mass = torch.empty(BH, p.G, p.N, dtype=torch.float32, device="cuda")
+    mcs.mcs_group_mass(p, q, k, lse, perm, 0, BH, mass)
+    idx = torch.empty(BH * p.G, p.K, dtype=torch.int32, device="cuda")
+    ret = torch.empty(BH * p.G, dtype=torch.float32, device="cuda")
+    mcs.mcs_topk(p, mass.view(-1, p.N), idx, ret)
+    assert mcs.mcs_device_status() == 0
+    return idx.view(p.B, p.H, p.G, p.K), ret.view(p.B, p.H, p.G)
+
+
+@pytest.mark.parametrize("case", ["small-s0.2", "ragged-K1", "ragged-K777", "ragged-KN"])
+def test_anchor_selection_matches_group_mass_plus_topk(case):
+    # The anchor step selects from the mass histogram in one read of the masses;
+    # mcs_group_mass + mcs_topk selects from the same masses in four reads.
+    # Both keep the K largest masses with ties to the lower index: the index
+    # sets must be identical.
+    if case == "small-s0.2":
+        w = synth.workload("small")
+        q, k, v = _dev(*synth.make_qkv(w, 0, heads=[0, 1]))
+        p = mcs.params(w.B, 2, w.N, w.D, w.C, w.K(0.2))
+    else:
+        N, D, C = 5001, 64, 64  # N % 4 != 0: mass rows are not 16-byte aligned
+        K = {"ragged-K1": 1, "ragged-K777": 777, "ragged-KN": N}[case]
+        q, k, v = _dev(*P.random_qkv(1, 2, N, D, seed=88))
+        p = mcs.params(1, 2, N, D, C, K)
+    perm, idx, lse, ret = _anchor(p, q, k, v)
+    idx2, ret2 = _two_pass_select(p, q, k, lse, perm)
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx2.cpu().numpy())
+    np.testing.assert_allclose(P.f64(ret), P.f64(ret2), rtol=1e-5)
+
+
+@pytest.mark.parametrize("N", [3000, 5000])
+def test_anchor_selection_all_masses_tied(N):
+    # K = 0: every score is 0, so every KV token has the same mass in every
+    # group; the lowest K indices win.  N = 3000 keeps the whole tied bucket
+    # within the one-read path's candidate capacity (4096); N = 5000 exceeds
+    # it and takes the multi-pass path.
+    D, C, K = 128, 128, 1000
+    q, _, v = P.random_qkv(1, 1, N, D, seed=91)
+    k = torch.zeros_like(q)
+    p = mcs.params(1, 1, N, D, C, K)
+    qd, kd, vd = _dev(q, k, v)
+    _, idx, _, ret = _anchor(p, qd, kd, vd)
+    want = np.broadcast_to(np.arange(K), (p.G, K))
+    np.testing.assert_array_equal(idx[0, 0].cpu().numpy(), want)
+    sizes = np.array([min(C, N - g * C) for g in range(p.G)])
+    np.testing.assert_allclose(P.f64(ret[0, 0]), sizes * K / N, rtol=1e-4)
+
+
 def test_anchor_then_reuse_identities_tiny_workload():
     w = synth.workload("tiny")
     K = w.K(0.2)

@@ -54,6 +54,7 @@ struct MassArgs {
   const int32_t* perm;    // [BH, G*C]
   const float* lse;       // [BH, N]
   float* mass;            // [heads in chunk, G, N]
+  uint32_t* hist;         // [heads in chunk, G, 2048] digit counts of each mass row, or null
   unsigned* status;
 };
 
@@ -62,8 +63,10 @@ cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* t
                               const MassArgs& a, int heads, cudaStream_t stream);
 
 // rows x n masses -> rows x K ascending indices (+ retained sums, nullable).
-cudaError_t launch_topk(const float* mass, int rows, int n, int K, int32_t* idx, float* retained,
-                        unsigned* status, cudaStream_t stream);
+// hist (nullable): each row's 2048-bin digit histogram written by the mass
+// kernel; with it most rows are selected in one read of their masses.
+cudaError_t launch_topk(const float* mass, const uint32_t* hist, int rows, int n, int K,
+                        int32_t* idx, float* retained, unsigned* status, cudaStream_t stream);
 
 // Device address of the library's status word (for kernels' status argument).
 cudaError_t device_status_word(unsigned** out);

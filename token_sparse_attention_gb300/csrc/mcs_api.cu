@@ -149,6 +149,51 @@ size_t mass_head_bytes(const mcs_params* p) {
   return static_cast<size_t>(groups_of(p)) * static_cast<size_t>(p->N) * sizeof(float);
 }
 
+// Workspace per head of the anchor step's selection: the group masses and
+// their 2048-bin digit histograms.
+constexpr size_t kHistBins = 2048;
+size_t hist_head_bytes(const mcs_params* p) {
+  return static_cast<size_t>(groups_of(p)) * kHistBins * sizeof(uint32_t);
+}
+size_t select_head_bytes(const mcs_params* p) {
+  return round_up(mass_head_bytes(p), 256) + round_up(hist_head_bytes(p), 256);
+}
+
+// a3 for heads [h0, h0 + hc), with (hist != null) or without the histograms.
+mcs_status run_group_mass(const mcs_params* p, const void* q, const void* k, const float* lse,
+                          const int32_t* perm, int h0, int hc, float* mass, uint32_t* hist,
+                          cudaStream_t stream) {
+  const int BH = p->B * p->H;
+  CUtensorMap tq, tk;
+  if (!make_gather_map(&tq, q, BH, p->N, p->D) || !make_tile_map(&tk, k, BH, p->N, p->D))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(mass)");
+  mcs::MassArgs a{};
+  a.N = p->N;
+  a.C = p->C;
+  a.G = groups_of(p);
+  a.head0 = h0;
+  a.scale_log2 = scale_of(p) * kLog2e;
+  a.perm = perm;
+  a.lse = lse;
+  a.mass = mass;
+  a.hist = hist;
+  mcs_status s;
+  if ((s = status_ptr(&a.status)) != MCS_OK) return s;
+  cudaError_t e = mcs::launch_group_mass(p->D, &tq, &tk, a, hc, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "group mass launch");
+  return MCS_OK;
+}
+
+mcs_status run_topk(const mcs_params* p, const float* mass, const uint32_t* hist, int rows,
+                    int32_t* idx, float* retained, cudaStream_t stream) {
+  unsigned* st;
+  mcs_status s;
+  if ((s = status_ptr(&st)) != MCS_OK) return s;
+  cudaError_t e = mcs::launch_topk(mass, hist, rows, p->N, p->K, idx, retained, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return MCS_OK;
+}
+
 }  // namespace
 
 namespace mcs {
@@ -200,7 +245,7 @@ size_t mcs_group_workspace(const mcs_params* p) {
 
 size_t mcs_anchor_workspace(const mcs_params* p) {
   if (check_shape(p, false) != MCS_OK) return 0;
-  const size_t per_head = round_up(mass_head_bytes(p), 256);
+  const size_t per_head = select_head_bytes(p);
   const size_t BH = static_cast<size_t>(p->B) * p->H;
   size_t heads = std::max<size_t>(1, (size_t(1) << 32) / per_head);
   heads = std::min(heads, BH);
@@ -265,34 +310,14 @@ mcs_status mcs_group_mass(const mcs_params* p, const void* q, const void* k, con
   if (!aligned16(q) || !aligned16(k)) return MCS_ERR_INVALID_ARG;
   const int BH = p->B * p->H;
   if (head_begin < 0 || head_count < 1 || head_begin + head_count > BH) return MCS_ERR_INVALID_ARG;
-  CUtensorMap tq, tk;
-  if (!make_gather_map(&tq, q, BH, p->N, p->D) || !make_tile_map(&tk, k, BH, p->N, p->D))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(mass)");
-  mcs::MassArgs a{};
-  a.N = p->N;
-  a.C = p->C;
-  a.G = groups_of(p);
-  a.head0 = head_begin;
-  a.scale_log2 = scale_of(p) * kLog2e;
-  a.perm = perm;
-  a.lse = lse;
-  a.mass = mass;
-  if ((s = status_ptr(&a.status)) != MCS_OK) return s;
-  cudaError_t e = mcs::launch_group_mass(p->D, &tq, &tk, a, head_count, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "group mass launch");
-  return MCS_OK;
+  return run_group_mass(p, q, k, lse, perm, head_begin, head_count, mass, nullptr, stream);
 }
 
 mcs_status mcs_topk(const mcs_params* p, const float* mass, int rows, int32_t* idx,
                     float* retained, cudaStream_t stream) {
   if (p == nullptr || p->N < 1 || p->K < 1 || p->K > p->N) return MCS_ERR_INVALID_ARG;
   if (rows < 0 || (rows > 0 && (!mass || !idx))) return MCS_ERR_INVALID_ARG;
-  unsigned* st;
-  mcs_status s;
-  if ((s = status_ptr(&st)) != MCS_OK) return s;
-  cudaError_t e = mcs::launch_topk(mass, rows, p->N, p->K, idx, retained, st, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
-  return MCS_OK;
+  return run_topk(p, mass, nullptr, rows, idx, retained, stream);
 }
 
 mcs_status mcs_sparse_attn(const mcs_params* p, const void* q, const void* k, const void* v,
@@ -308,6 +333,33 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
   return run_sparse(p, q, k, v, perm, idx, dense_out, residual, mcs::kSparseRecord, stream);
 }
 
+mcs_status mcs_select(const mcs_params* p, const void* q, const void* k, const float* lse,
+                      const int32_t* perm, int32_t* idx, float* retained, void* ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+  mcs_status s = check_shape(p, true);
+  if (s != MCS_OK) return s;
+  if (!q || !k || !lse || !perm || !idx) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k)) return MCS_ERR_INVALID_ARG;
+  const size_t per_head = select_head_bytes(p);
+  if (!ws || !aligned16(ws) || ws_bytes < per_head) return MCS_ERR_WORKSPACE;
+  const int BH = p->B * p->H;
+  const int G = groups_of(p);
+  // a chunk of heads at a time through the workspace: the masses [chunk, G, N],
+  // then their digit histograms [chunk, G, 2048]
+  const int chunk = static_cast<int>(std::min<size_t>(BH, ws_bytes / per_head));
+  float* mass = static_cast<float*>(ws);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) +
+                                               round_up(chunk * mass_head_bytes(p), 256));
+  for (int h0 = 0; h0 < BH; h0 += chunk) {
+    const int hc = std::min(chunk, BH - h0);
+    if ((s = run_group_mass(p, q, k, lse, perm, h0, hc, mass, hist, stream)) != MCS_OK) return s;
+    int32_t* idx_h = idx + static_cast<size_t>(h0) * G * p->K;
+    float* ret_h = retained ? retained + static_cast<size_t>(h0) * G : nullptr;
+    if ((s = run_topk(p, mass, hist, hc * G, idx_h, ret_h, stream)) != MCS_OK) return s;
+  }
+  return MCS_OK;
+}
+
 mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, const void* v,
                              int32_t* perm, int32_t* idx, void* dense_out, float* lse,
                              void* residual, float* retained, void* ws, size_t ws_bytes,
@@ -316,25 +368,14 @@ mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, 
   if (s != MCS_OK) return s;
   if (!q || !k || !v || !perm || !idx || !dense_out || !lse || !residual)
     return MCS_ERR_INVALID_ARG;
-  const size_t per_head = round_up(mass_head_bytes(p), 256);
-  if (!ws || !aligned16(ws) || ws_bytes < std::max(per_head, mcs_group_workspace(p)))
+  if (!ws || !aligned16(ws) || ws_bytes < std::max(select_head_bytes(p), mcs_group_workspace(p)))
     return MCS_ERR_WORKSPACE;
-  const int BH = p->B * p->H;
-  const int G = groups_of(p);
   // a1
   if ((s = mcs_group(p, q, perm, ws, ws_bytes, stream)) != MCS_OK) return s;
   // a2
   if ((s = mcs_dense_attn(p, q, k, v, dense_out, lse, stream)) != MCS_OK) return s;
-  // a3 + a4, a chunk of heads at a time through the workspace
-  const int chunk = static_cast<int>(std::min<size_t>(BH, ws_bytes / per_head));
-  float* mass = static_cast<float*>(ws);
-  for (int h0 = 0; h0 < BH; h0 += chunk) {
-    const int hc = std::min(chunk, BH - h0);
-    if ((s = mcs_group_mass(p, q, k, lse, perm, h0, hc, mass, stream)) != MCS_OK) return s;
-    int32_t* idx_h = idx + static_cast<size_t>(h0) * G * p->K;
-    float* ret_h = retained ? retained + static_cast<size_t>(h0) * G : nullptr;
-    if ((s = mcs_topk(p, mass, hc * G, idx_h, ret_h, stream)) != MCS_OK) return s;
-  }
+  // a3 + a4
+  if ((s = mcs_select(p, q, k, lse, perm, idx, retained, ws, ws_bytes, stream)) != MCS_OK) return s;
   // a5, anchor form
   return mcs_sparse_attn_record(p, q, k, v, perm, idx, dense_out, residual, stream);
 }

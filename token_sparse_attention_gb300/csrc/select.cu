@@ -17,11 +17,17 @@
 // Two K stages and two TMEM score buffers let the MMA of tile j+1 run while
 // tile j is exponentiated.
 //
-// topk_kernel: one CTA per (head, group) row of masses.  Radix select of the
-// K-th largest value on the float bit pattern (masses are >= 0, so unsigned
-// order of the bits is numeric order), 12+12+8-bit digits, then one ordered
-// compaction pass that keeps every larger value and the lowest-index ties,
-// writing indices ascending.
+// Top-K: one CTA per (head, group) row of masses, selecting on the float bit
+// pattern (masses are >= 0, so unsigned order of the bits is numeric order),
+// ties to the lower index, indices written ascending.  Within the anchor step
+// the mass kernel also counts each row's masses by their top 12 bits; from
+// that histogram topk_hist_kernel knows the bucket of the K-th largest mass
+// before it reads the row, and selects in one read of the masses.  (The
+// second pass fuses group aggregation with top-K: ai.info AI summary,
+// "Methodology in Plain English".  The masses still go through HBM here: one
+// row of N fp32 masses does not fit in shared memory.)
+// topk_kernel (no histogram) runs a 12+12+8-bit radix select and an ordered
+// compaction: four reads of the row.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -29,6 +35,13 @@ namespace mcs {
 namespace {
 
 constexpr int kMassThreads = 192;
+// Histogram digit of a mass: the float's top 12 bits (sign, exponent, three
+// mantissa bits; masses are >= 0, so the digit grows with the mass), clamped
+// so that a NaN with the sign bit set stays in range.
+constexpr int kHistBins = 2048;
+__device__ __forceinline__ uint32_t mass_digit(uint32_t bits) {
+  return min(bits >> 20, static_cast<uint32_t>(kHistBins - 1));
+}
 
 template <int D, int CQ>
 struct MassLayout {
@@ -39,7 +52,8 @@ struct MassLayout {
   static constexpr int kK0 = kSub * kQSub;      // 1024-aligned (CQ multiple of 8)
   static constexpr int kKStage = kSub * kKSub;
   static constexpr int kBias = kK0 + 2 * kKStage;
-  static constexpr int kBars = kBias + CQ * 4;
+  static constexpr int kHist = kBias + CQ * 4;           // mass histogram (kHistBins words)
+  static constexpr int kBars = kHist + kHistBins * 4;
   static constexpr int kUsed = kBars + 128 + 1024;
   // at most two CTAs per SM (TMEM: 2 x 256 columns)
   static constexpr int kSmem = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
@@ -70,6 +84,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
   uint8_t* sq = smem + L::kQ;
   uint8_t* sk = smem + L::kK0;
   float* bias = reinterpret_cast<float*>(smem + L::kBias);
+  uint32_t* shist = reinterpret_cast<uint32_t*>(smem + L::kHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;   // [2]
@@ -186,6 +201,8 @@ __global__ void __launch_bounds__(kMassThreads, 2)
       bias[t] = (p >= 0 && p < a.N) ? __ldg(a.lse + static_cast<size_t>(bh) * a.N + p) * kLog2e
                                     : INFINITY;
     }
+    if (a.hist != nullptr)
+      for (int b = t; b < kHistBins; b += 128) shist[b] = 0;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const float sl2 = a.scale_log2;
     float* mass_row = a.mass + (static_cast<size_t>(hc) * a.G + g) * a.N;
@@ -213,7 +230,15 @@ __global__ void __launch_bounds__(kMassThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + st);
       const int jrow = j * 128 + t;
-      if (jrow < a.N) mass_row[jrow] = acc;
+      if (jrow < a.N) {
+        mass_row[jrow] = acc;
+        if (a.hist != nullptr) atomicAdd(&shist[mass_digit(__float_as_uint(acc))], 1u);
+      }
+    }
+    if (a.hist != nullptr) {
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      uint32_t* hist_row = a.hist + (static_cast<size_t>(hc) * a.G + g) * kHistBins;
+      for (int b = t; b < kHistBins; b += 128) hist_row[b] = shist[b];
     }
   }
 
@@ -237,6 +262,10 @@ cudaError_t launch_mass_one(const CUtensorMap* tq, const CUtensorMap* tk, const 
 // ---------------------------------------------------------------- top-K
 
 constexpr int kTopkThreads = 1024;
+// Candidate capacity of the one-read path: rows whose threshold bucket holds
+// more masses than this (ties en masse, degenerate inputs) take the
+// multi-pass path instead.
+constexpr int kCandCap = 4096;
 
 // Inclusive scan over the block of a packed value; returns the block total in *total.
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_sums,
@@ -265,21 +294,44 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
   return v + before;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_kernel(const float* __restrict__ mass, int n, int K, int32_t* __restrict__ idx,
-                float* __restrict__ retained, unsigned* status) {
-  __shared__ uint32_t hist[4096];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ uint32_t sel_digit, sel_above;
-  __shared__ float red[32];
+// Block sum of acc, stored to *dst by thread 0 (every thread must call).
+__device__ __forceinline__ void block_sum_store(float acc, float* red, float* dst) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = red[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) *dst = v;
+  }
+}
 
+// Number of entries of the ascending array a[0, n) below x.
+__device__ __forceinline__ uint32_t count_below(const uint32_t* a, uint32_t n, uint32_t x) {
+  uint32_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// One row, multi-pass: radix select of the K-th largest key in 12+12+8-bit
+// digits (three reads of the row), then one ordered compaction (a fourth
+// read) that keeps every larger key and the lowest-index ties.  hist holds
+// 4096 words, scal 2.
+__device__ void topk_row_multipass(const uint32_t* __restrict__ keys, int n, int K,
+                                   int32_t* __restrict__ out, float* retained_row, unsigned* status,
+                                   uint32_t* hist, uint32_t* warp_sums, uint32_t* scal,
+                                   float* red) {
   const int tid = threadIdx.x;
-  const size_t row = blockIdx.x;
-  const uint32_t* keys = reinterpret_cast<const uint32_t*>(mass + row * n);
-
   uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(K);
   const int shifts[3] = {20, 8, 0};
   const int widths[3] = {12, 12, 8};
+#pragma unroll
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass];
     const int nb = 1 << widths[pass];
@@ -303,16 +355,16 @@ __global__ void __launch_bounds__(kTopkThreads)
       for (int q = 0; q < per; ++q) {
         const uint32_t c = hist[first - q];
         if (above < remaining && remaining <= above + c) {
-          sel_digit = static_cast<uint32_t>(first - q);
-          sel_above = above;
+          scal[0] = static_cast<uint32_t>(first - q);
+          scal[1] = above;
         }
         above += c;
       }
     }
     __syncthreads();
-    prefix |= sel_digit << shift;
+    prefix |= scal[0] << shift;
     prefix_mask |= static_cast<uint32_t>(nb - 1) << shift;
-    remaining -= sel_above;
+    remaining -= scal[1];
     __syncthreads();
   }
   // prefix == the K-th largest key; take every larger key and the first
@@ -321,7 +373,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   const uint32_t need_eq = remaining;
   uint32_t run_gt = 0, run_eq = 0;
   float acc = 0.f;
-  int32_t* out = idx + row * K;
   for (int base = 0; base < n; base += kTopkThreads) {
     const int i = base + tid;
     uint32_t k = 0;
@@ -349,20 +400,236 @@ __global__ void __launch_bounds__(kTopkThreads)
     run_gt += total >> 16;
     run_eq += total & 0xFFFFu;
   }
-  if (retained != nullptr) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if ((tid & 31) == 0) red[tid >> 5] = acc;
-    __syncthreads();
-    if (tid < 32) {
-      float v = red[tid];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (tid == 0) retained[row] = v;
-    }
-  }
+  if (retained_row != nullptr) block_sum_store(acc, red, retained_row);
 }
 
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_kernel(const float* __restrict__ mass, int n, int K, int32_t* __restrict__ idx,
+                float* __restrict__ retained, unsigned* status) {
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t scal[2];
+  __shared__ float red[32];
+  const size_t row = blockIdx.x;
+  topk_row_multipass(reinterpret_cast<const uint32_t*>(mass + row * n), n, K, idx + row * K,
+                     retained ? retained + row : nullptr, status, hist, warp_sums, scal, red);
+}
+
+// Dynamic shared memory of topk_hist_kernel, in 32-bit words.
+__host__ __device__ constexpr int topk_hist_words(int K) { return 72 + 1024 + K + 2 * kCandCap; }
+
+// One row per CTA, given the row's digit histogram (mass_digit counts).
+//  1. From the histogram: the digit d of the K-th largest mass and the count A
+//     of masses with a larger digit; the M masses of digit d are candidates.
+//  2. One read of the row: indices of digit > d go, in order, to above[0, A);
+//     candidates (key, index), in order, to ckey/cidx.
+//  3. Radix select over the candidates' 20 low bits (two 10-bit digits) gives
+//     the K-th largest key T and how many keys equal to T to keep; the kept
+//     candidates are compacted in order (larger keys, then the lowest-index
+//     ties).
+//  4. The two ascending index lists are merged into the output.
+// A row whose bucket exceeds kCandCap, whose digit is the clamped top one, or
+// whose masses do not match the histogram takes topk_row_multipass.
+__global__ void __launch_bounds__(kTopkThreads, 2)
+    topk_hist_kernel(const float* __restrict__ mass, const uint32_t* __restrict__ hist, int n,
+                     int K, int32_t* __restrict__ idx, float* __restrict__ retained,
+                     unsigned* status) {
+  extern __shared__ uint32_t tsm[];
+  uint32_t* warp_sums = tsm;                        // 32
+  uint32_t* scal = tsm + 32;                        // 8
+  float* red = reinterpret_cast<float*>(tsm + 40);  // 32
+  uint32_t* h = tsm + 72;                           // 1024 (and 4096 for the fallback)
+  uint32_t* above = h + 1024;                       // K
+  uint32_t* ckey = above + K;                       // kCandCap
+  uint32_t* cidx = ckey + kCandCap;                 // kCandCap
+
+  const int tid = threadIdx.x;
+  const size_t row = blockIdx.x;
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(mass + row * n);
+  int32_t* out = idx + row * K;
+  float* ret_row = retained ? retained + row : nullptr;
+  const uint32_t uK = static_cast<uint32_t>(K);
+
+  // 1. threshold digit (two bins per thread, counted from the top)
+  const uint32_t* hrow = hist + row * kHistBins;
+  const int first = kHistBins - 1 - 2 * tid;
+  const uint32_t c0 = hrow[first], c1 = hrow[first - 1];
+  if (tid == 0) {
+    scal[0] = kHistBins;  // not found
+    scal[1] = 0;
+  }
+  uint32_t total;
+  const uint32_t incl = block_inclusive_scan(c0 + c1, warp_sums, &total);
+  const uint32_t ab = incl - (c0 + c1);
+  if (ab < uK && uK <= ab + c0) {
+    scal[0] = first;
+    scal[1] = ab;
+  } else if (ab + c0 < uK && uK <= ab + c0 + c1) {
+    scal[0] = first - 1;
+    scal[1] = ab + c0;
+  }
+  __syncthreads();
+  const uint32_t d = scal[0], A = scal[1];
+  const uint32_t M = d < kHistBins ? hrow[d] : 0u;
+  bool fast = d < kHistBins - 1 && M <= kCandCap && total == static_cast<uint32_t>(n);
+
+  // 2. one read of the row, eight contiguous masses per thread per chunk (two
+  // 16-byte loads in flight per thread)
+  float acc = 0.f;
+  if (fast) {
+    const bool vec = (reinterpret_cast<uintptr_t>(keys) & 15) == 0;
+    constexpr int kPer = 8;
+    auto load = [&](int i0, uint32_t* u) {
+      if (vec && i0 + kPer - 1 < n) {
+        const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(keys + i0));
+        const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(keys + i0 + 4));
+        u[0] = v0.x;
+        u[1] = v0.y;
+        u[2] = v0.z;
+        u[3] = v0.w;
+        u[4] = v1.x;
+        u[5] = v1.y;
+        u[6] = v1.z;
+        u[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) u[e] = i0 + e < n ? __ldg(keys + i0 + e) : 0u;
+      }
+    };
+    constexpr int kChunk = kPer * kTopkThreads;
+    uint32_t run_a = 0, run_c = 0;
+    for (int base = 0; base < n; base += kChunk) {
+      const int i0 = base + kPer * tid;
+      uint32_t cur[kPer];
+      load(i0, cur);
+      uint32_t na = 0, nc = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const bool valid = i0 + e < n;
+        const uint32_t dg = mass_digit(cur[e]);
+        na += (valid && dg > d) ? 1u : 0u;
+        nc += (valid && dg == d) ? 1u : 0u;
+      }
+      const uint32_t packed = (na << 16) | nc;
+      uint32_t tot;
+      const uint32_t excl = block_inclusive_scan(packed, warp_sums, &tot) - packed;
+      uint32_t pa = run_a + (excl >> 16), pc = run_c + (excl & 0xFFFFu);
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        if (i0 + e >= n) continue;
+        const uint32_t dg = mass_digit(cur[e]);
+        if (dg > d) {
+          if (pa < A) above[pa] = static_cast<uint32_t>(i0 + e);
+          ++pa;
+          acc += __uint_as_float(cur[e]);
+        } else if (dg == d) {
+          if (pc < M) {
+            ckey[pc] = cur[e];
+            cidx[pc] = static_cast<uint32_t>(i0 + e);
+          }
+          ++pc;
+        }
+      }
+      run_a += tot >> 16;
+      run_c += tot & 0xFFFFu;
+    }
+    // block-uniform: the histogram must describe exactly these masses
+    fast = run_a == A && run_c == M;
+  }
+  __syncthreads();
+  if (!fast) {
+    topk_row_multipass(keys, n, K, out, ret_row, status, h, warp_sums, scal, red);
+    return;
+  }
+
+  // 3. the (K - A)-th largest candidate key, two 10-bit digits below d
+  uint32_t pref = d << 20, pmask = 0xFFF00000u, R = uK - A;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    h[tid] = 0;
+    __syncthreads();
+    for (uint32_t c = tid; c < M; c += kTopkThreads) {
+      const uint32_t u = ckey[c];
+      if ((u & pmask) == pref) atomicAdd(&h[(u >> shift) & 1023u], 1u);
+    }
+    __syncthreads();
+    const uint32_t bin = 1023u - tid;
+    const uint32_t mine = h[bin];
+    uint32_t tot;
+    const uint32_t below = block_inclusive_scan(mine, warp_sums, &tot) - mine;
+    if (below < R && R <= below + mine) {
+      scal[2] = bin;
+      scal[3] = below;
+    }
+    __syncthreads();
+    pref |= scal[2] << shift;
+    pmask |= 1023u << shift;
+    R -= scal[3];
+    __syncthreads();
+  }
+  // keep candidates > T and the first need_eq equal to T, compacted in place
+  // (a kept candidate moves to a position no later than its own)
+  const uint32_t T = pref, need_eq = R;
+  uint32_t run_gt = 0, run_eq = 0;
+  for (uint32_t base = 0; base < M; base += kTopkThreads) {
+    const uint32_t c = base + tid;
+    uint32_t u = 0, id = 0;
+    bool gt = false, eq = false;
+    if (c < M) {
+      u = ckey[c];
+      id = cidx[c];
+      gt = u > T;
+      eq = u == T;
+    }
+    const uint32_t packed = (gt ? (1u << 16) : 0u) | (eq ? 1u : 0u);
+    uint32_t tot;
+    const uint32_t excl = block_inclusive_scan(packed, warp_sums, &tot) - packed;
+    const uint32_t gb = run_gt + (excl >> 16), eb = run_eq + (excl & 0xFFFFu);
+    if (gt || (eq && eb < need_eq)) {
+      cidx[gb + min(eb, need_eq)] = id;
+      acc += __uint_as_float(u);
+    }
+    run_gt += tot >> 16;
+    run_eq += tot & 0xFFFFu;
+  }
+  __syncthreads();
+
+  // 4. merge the ascending lists above[0, A) and cidx[0, Rk) into out[0, K)
+  // The kept candidates go to their final slots (binary search in the above
+  // list) and mark them in a bitmap over out; every other slot p then takes
+  // above[p - (marked slots before p)], found from per-word prefix counts.
+  const uint32_t Rk = uK - A;
+  if (run_gt + min(run_eq, need_eq) != Rk) atomicOr(status, DEV_BOUNDS);  // cannot happen
+  const uint32_t nw = (uK + 31) / 32;  // <= kCandCap / 2 whenever this path runs
+  uint32_t* bits = ckey;               // the candidate keys are no longer needed
+  uint32_t* wpre = ckey + nw;
+  for (uint32_t w = tid; w < nw; w += kTopkThreads) bits[w] = 0;
+  __syncthreads();
+  for (uint32_t q = tid; q < Rk; q += kTopkThreads) {
+    const uint32_t x = cidx[q];
+    const uint32_t f = q + count_below(above, A, x);
+    out[f] = static_cast<int32_t>(x);
+    atomicOr(&bits[f >> 5], 1u << (f & 31));
+  }
+  __syncthreads();
+  uint32_t run = 0;
+  for (uint32_t base = 0; base < nw; base += kTopkThreads) {
+    const uint32_t w = base + tid;
+    const uint32_t c = w < nw ? static_cast<uint32_t>(__popc(bits[w])) : 0u;
+    uint32_t tot;
+    const uint32_t incl = block_inclusive_scan(c, warp_sums, &tot);
+    if (w < nw) wpre[w] = run + incl - c;
+    run += tot;
+  }
+  __syncthreads();
+  for (uint32_t pos = tid; pos < uK; pos += kTopkThreads) {
+    const uint32_t word = bits[pos >> 5], bit = 1u << (pos & 31);
+    if ((word & bit) == 0u)
+      out[pos] = static_cast<int32_t>(
+          above[pos - (wpre[pos >> 5] + static_cast<uint32_t>(__popc(word & (bit - 1u))))]);
+  }
+  if (ret_row != nullptr) block_sum_store(acc, red, ret_row);
+}
 }  // namespace
 
 cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* tk,
@@ -374,9 +641,18 @@ cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* t
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_topk(const float* mass, int rows, int n, int K, int32_t* idx, float* retained,
-                        unsigned* status, cudaStream_t stream) {
+cudaError_t launch_topk(const float* mass, const uint32_t* hist, int rows, int n, int K,
+                        int32_t* idx, float* retained, unsigned* status, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(topk_hist_words(K)) * 4;
+  if (hist != nullptr && smem <= 227 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_hist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_hist_kernel<<<rows, kTopkThreads, smem, stream>>>(mass, hist, n, K, idx, retained, status);
+    return cudaGetLastError();
+  }
   topk_kernel<<<rows, kTopkThreads, 0, stream>>>(mass, n, K, idx, retained, status);
   return cudaGetLastError();
 }

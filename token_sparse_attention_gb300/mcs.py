@@ -20,7 +20,7 @@ __all__ = [
     "McsError", "Params", "params", "lib", "library_path", "EXPORTED",
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status",
     "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
-    "mcs_group_mass", "mcs_topk", "mcs_sparse_attn", "mcs_sparse_attn_record",
+    "mcs_group_mass", "mcs_topk", "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record",
     "mcs_anchor_select", "mcs_group_noalloc",
 ]
 
@@ -28,7 +28,7 @@ __all__ = [
 EXPORTED = (
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
-    "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
+    "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
 )
 
 STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
@@ -77,6 +77,7 @@ _SIGS = {
     "mcs_dense_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_group_mass": ([_pp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp], _st),
     "mcs_topk": ([_pp, _vp, _i, _vp, _vp, _vp], _st),
+    "mcs_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
     "mcs_sparse_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_sparse_attn_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_anchor_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
@@ -220,6 +221,17 @@ def mcs_sparse_attn_record(p: Params, q, k, v, perm, idx, dense_out, residual, s
         _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
         _ptr(dense_out, bf, s, "dense_out"), _ptr(residual, bf, s, "residual"),
         _stream(stream)), "mcs_sparse_attn_record")
+
+
+def mcs_select(p: Params, q, k, lse, perm, idx, ws, retained=None, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_select(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
+        _ptr(lse, torch.float32, s[:3], "lse"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(retained, torch.float32, (p.B, p.H, p.G), "retained", optional=True),
+        _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)), "mcs_select")
 
 
 def mcs_anchor_select(p: Params, q, k, v, perm, idx, dense_out, lse, residual, ws,
