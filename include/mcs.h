@@ -29,7 +29,9 @@
  *    Kernels never trap.
  *  - The library allocates no memory.  Entry points that need scratch take
  *    a caller-provided device workspace (size from the *_workspace queries).
- *    Apart from the device status word it holds no state between calls.
+ *    Apart from the device status word and the stager objects the caller
+ *    creates and destroys (mcs_stager_*: a few CUDA events each) it holds no
+ *    state between calls.
  *  - Supported: D in {64, 128}, C in {64, 128}, 1 <= K <= N, B*H <= 65535.
  */
 #ifndef MCS_H_
@@ -211,6 +213,59 @@ mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, 
  */
 mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int32_t* perm,
                              cudaStream_t stream);
+
+/*
+ * Metadata cache staging between host and device memory.  A layer's cached
+ * metadata (groups, KV indices, residual) is produced at the anchor and read
+ * at every reuse step of that layer; when device memory is short, entries of
+ * inactive layers live in host memory and are prefetched one layer ahead so
+ * that the copy hides behind the current layer's sparse attention (ai.info
+ * AI summary, "Main Findings", on cache transfers hiding behind computation;
+ * wispaper.ai, "Speedups come with negligible measured quality loss", on
+ * offloading inactive cache entries to CPU memory).
+ *
+ * An entry is one flat buffer of mcs_meta_bytes(p) bytes holding perm
+ * [B,H,G*C] int32, idx [B,H,G,K] int32 and residual [B,H,N,D] bf16, each at
+ * a 256-byte aligned offset (mcs_meta_offsets); host and device copies share
+ * the layout, so one copy moves an entry.  Both return 0 / MCS_ERR_* for
+ * invalid params (K must be in [1, N]).
+ */
+size_t mcs_meta_bytes(const mcs_params* p);
+mcs_status mcs_meta_offsets(const mcs_params* p, size_t* perm_off, size_t* idx_off,
+                            size_t* residual_off);
+
+typedef struct mcs_stager mcs_stager;
+
+/*
+ * Creates a stager over `slots` (>= 1) caller-owned device buffers of
+ * mcs_meta_bytes(p) bytes each (256-byte aligned; the array is copied),
+ * copying on the caller's `copy_stream`.  The stager owns one CUDA event per
+ * slot plus one, freed by mcs_stager_destroy.  Host entries should be pinned
+ * (page-locked) memory, or the copies are not asynchronous.  A stager is used
+ * from one host thread at a time.
+ */
+mcs_status mcs_stager_create(const mcs_params* p, int slots, void* const* device_slots,
+                             cudaStream_t copy_stream, mcs_stager** out);
+void mcs_stager_destroy(mcs_stager* s);
+
+/*
+ * Queues the copy host_entry -> device slot `slot` on the copy stream, to
+ * start once the work queued so far on `after` is done (pass the stream that
+ * last read the slot, so that the copy does not overwrite metadata still in
+ * use).  Returns without waiting.
+ */
+mcs_status mcs_stager_prefetch(mcs_stager* s, int slot, const void* host_entry,
+                               cudaStream_t after);
+
+/*
+ * Queues the copy device slot `slot` -> host_entry on the copy stream, to
+ * start once the work queued so far on `after` is done (pass the stream whose
+ * work wrote the slot, e.g. the anchor step's).
+ */
+mcs_status mcs_stager_offload(mcs_stager* s, int slot, void* host_entry, cudaStream_t after);
+
+/* Makes `stream` wait (on the device) for the slot's last queued copy. */
+mcs_status mcs_stager_wait(mcs_stager* s, int slot, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -86,3 +86,39 @@ def test_workspace_queries(L):
     assert a >= p.G * p.N * 4
     bad = mcs.params(1, 2, 2048, 96, 64, 410)
     assert mcs.mcs_group_workspace(bad) == 0
+
+
+def test_meta_entry_layout(L):
+    # one layer's cache entry: perm | idx | residual, 256-byte aligned sections
+    p = mcs.params(1, 40, 75600, 128, 128, 15120)
+    G = p.G
+    po, io, ro = mcs.mcs_meta_offsets(p)
+    total = mcs.mcs_meta_bytes(p)
+    perm_b, idx_b, res_b = 40 * G * 128 * 4, 40 * G * 15120 * 4, 40 * 75600 * 128 * 2
+    assert po == 0 and io % 256 == 0 and ro % 256 == 0 and total % 256 == 0
+    assert perm_b <= io < perm_b + 256
+    assert idx_b <= ro - io < idx_b + 256
+    assert res_b <= total - ro < res_b + 256
+    # K outside [1, N]: no size, an error status
+    bad = mcs.params(1, 1, 100, 128, 64, 0)
+    assert L.mcs_meta_bytes(ctypes.byref(bad)) == 0
+    assert L.mcs_meta_offsets(ctypes.byref(bad), None, None, None) == 1
+
+
+def test_stager_rejects_bad_arguments(L):
+    # every check here happens on the host before any CUDA call
+    p = mcs.params(1, 2, 256, 128, 64, 40)
+    h = ctypes.c_void_p()
+    two = (ctypes.c_void_p * 2)(256, 512)
+    assert L.mcs_stager_create(ctypes.byref(p), 2, two, None, None) == 1    # no out pointer
+    assert L.mcs_stager_create(ctypes.byref(p), 0, two, None, ctypes.byref(h)) == 1  # no slots
+    assert L.mcs_stager_create(ctypes.byref(p), 2, None, None, ctypes.byref(h)) == 1
+    odd = (ctypes.c_void_p * 1)(256 + 16)                                   # not 256-aligned
+    assert L.mcs_stager_create(ctypes.byref(p), 1, odd, None, ctypes.byref(h)) == 1
+    bad = mcs.params(1, 2, 256, 96, 64, 40)                                 # unsupported D
+    assert L.mcs_stager_create(ctypes.byref(bad), 2, two, None, ctypes.byref(h)) == 2
+    assert not h.value
+    assert L.mcs_stager_prefetch(None, 0, 16, None) == 1
+    assert L.mcs_stager_offload(None, 0, 16, None) == 1
+    assert L.mcs_stager_wait(None, 0, None) == 1
+    L.mcs_stager_destroy(None)

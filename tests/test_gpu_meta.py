@@ -1,0 +1,122 @@
+"""GPU tests of the metadata cache staging (mcs_meta_*, mcs_stager_*): entries
+offloaded to pinned host memory and prefetched back into device slots, one
+layer ahead, give the same reuse-step outputs as metadata kept on the device.
+Every call goes through the C ABI (libmcs.so)."""
+
+import numpy as np
+import pytest
+import torch
+
+from token_sparse_attention_gb300 import build as mcs_build
+from token_sparse_attention_gb300 import mcs
+from token_sparse_attention_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mcs_build.build()
+    mcs.lib()
+    assert torch.cuda.is_available()
+    yield
+    assert mcs.mcs_device_status() == 0
+
+
+def _anchor_into(p, q, k, v, entry):
+    """Anchor step whose perm / idx / residual land in a device entry."""
+    perm, idx, res = mcs.meta_views(p, entry)
+    dense = torch.empty_like(q)
+    lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device="cuda")
+    ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+    mcs.mcs_anchor_select(p, q, k, v, perm, idx, dense, lse, res, ws)
+
+
+def _layer_inputs(w, layer):
+    # each layer has its own activations: the workload's generator at step
+    # `layer` (anchor) and `layer + 1` (reuse)
+    q0, k0, v0 = [t.cuda() for t in synth.make_qkv(w, layer)]
+    q1, k1, v1 = [t.cuda() for t in synth.make_qkv(w, layer + 1)]
+    return (q0, k0, v0), (q1, k1, v1)
+
+
+def test_offload_prefetch_round_trip():
+    w = synth.workload("tiny")
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
+    nbytes = mcs.mcs_meta_bytes(p)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    (q0, k0, v0), _ = _layer_inputs(w, 0)
+    _anchor_into(p, q0, k0, v0, dev)
+    want = dev.clone()
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    copy = torch.cuda.Stream()
+    st = mcs.Stager(p, [dev], copy)
+    cur = torch.cuda.current_stream()
+    st.offload(0, host, after=cur)
+    st.wait(0, cur)
+    dev.zero_()               # queued on the compute stream after the offload
+    st.prefetch(0, host, after=cur)
+    st.wait(0, cur)
+    got = dev.clone()         # ordered after the prefetch by the wait
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    perm, idx, res = mcs.meta_views(p, host)
+    assert torch.equal(idx, mcs.meta_views(p, want.cpu())[1])
+    st.close()
+
+
+def test_layer_pipeline_prefetch_one_ahead_matches_resident():
+    # three layers, two device slots: while layer l runs from slot l % 2 the
+    # entry of layer l + 1 is copied into the other slot
+    w = synth.workload("tiny")
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
+    L = 3
+    nbytes = mcs.mcs_meta_bytes(p)
+    resident, hosts, reuse_in = [], [], []
+    for layer in range(L):
+        (q0, k0, v0), (q1, k1, v1) = _layer_inputs(w, 2 * layer)
+        e = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        _anchor_into(p, q0, k0, v0, e)
+        resident.append(e)
+        reuse_in.append((q1, k1, v1))
+    copy = torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    # offload each layer's entry to pinned host memory through one slot
+    tmp = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    off = mcs.Stager(p, [tmp], copy)
+    for layer in range(L):
+        h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        tmp.copy_(resident[layer])
+        off.offload(0, h, after=cur)
+        off.wait(0, cur)        # tmp is reused next iteration
+        hosts.append(h)
+    torch.cuda.synchronize()
+    off.close()
+    # resident reference outputs
+    want = []
+    for layer in range(L):
+        perm, idx, res = mcs.meta_views(p, resident[layer])
+        q1, k1, v1 = reuse_in[layer]
+        out = torch.empty_like(q1)
+        mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idx, res, out)
+        want.append(out)
+    # staged: two slots, prefetch one layer ahead
+    slots = [torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = mcs.Stager(p, slots, copy)
+    st.prefetch(0, hosts[0], after=cur)
+    got = []
+    for layer in range(L):
+        s = layer % 2
+        if layer + 1 < L:
+            st.prefetch(1 - s, hosts[layer + 1], after=cur)
+        st.wait(s, cur)
+        perm, idx, res = mcs.meta_views(p, slots[s])
+        q1, k1, v1 = reuse_in[layer]
+        out = torch.empty_like(q1)
+        mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idx, res, out)
+        got.append(out)
+    torch.cuda.synchronize()
+    st.close()
+    for layer in range(L):
+        np.testing.assert_array_equal(got[layer].view(torch.int16).cpu().numpy(),
+                                      want[layer].view(torch.int16).cpu().numpy())

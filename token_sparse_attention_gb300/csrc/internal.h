@@ -7,7 +7,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "mcs.h"
+
 namespace mcs {
+
+// Records "what: <CUDA error string>" as the thread's last CUDA error and
+// returns MCS_ERR_CUDA.
+mcs_status record_cuda_error(cudaError_t e, const char* what);
+// The shape checks every entry point applies (need_k: K must be in [1, N]).
+mcs_status check_params(const mcs_params* p, bool need_k);
 
 // Device status bits, OR-ed into the library's status word.
 enum : unsigned {

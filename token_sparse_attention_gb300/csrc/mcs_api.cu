@@ -197,6 +197,10 @@ mcs_status run_topk(const mcs_params* p, const float* mass, const uint32_t* hist
 }  // namespace
 
 namespace mcs {
+
+mcs_status record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+mcs_status check_params(const mcs_params* p, bool need_k) { return check_shape(p, need_k); }
+
 cudaError_t device_status_word(unsigned** out) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_mcs_status);
 }

@@ -21,7 +21,8 @@ __all__ = [
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status",
     "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
     "mcs_group_mass", "mcs_topk", "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record",
-    "mcs_anchor_select", "mcs_group_noalloc",
+    "mcs_anchor_select", "mcs_group_noalloc", "mcs_meta_bytes", "mcs_meta_offsets",
+    "meta_views", "Stager",
 ]
 
 # Every symbol include/mcs.h declares.
@@ -29,6 +30,8 @@ EXPORTED = (
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
     "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
+    "mcs_meta_bytes", "mcs_meta_offsets", "mcs_stager_create", "mcs_stager_destroy",
+    "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait",
 )
 
 STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
@@ -82,6 +85,13 @@ _SIGS = {
     "mcs_sparse_attn_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_anchor_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
     "mcs_group_noalloc": ([_pp, _vp, _vp, _vp], _st),
+    "mcs_meta_bytes": ([_pp], _sz),
+    "mcs_meta_offsets": ([_pp, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)], _st),
+    "mcs_stager_create": ([_pp, _i, ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp)], _st),
+    "mcs_stager_destroy": ([_vp], None),
+    "mcs_stager_prefetch": ([_vp, _i, _vp, _vp], _st),
+    "mcs_stager_offload": ([_vp, _i, _vp, _vp], _st),
+    "mcs_stager_wait": ([_vp, _i, _vp], _st),
 }
 
 
@@ -245,6 +255,77 @@ def mcs_anchor_select(p: Params, q, k, v, perm, idx, dense_out, lse, residual, w
         _ptr(residual, bf, s, "residual"),
         _ptr(retained, torch.float32, (p.B, p.H, p.G), "retained", optional=True),
         _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)), "mcs_anchor_select")
+
+
+def mcs_meta_bytes(p: Params) -> int:
+    return lib().mcs_meta_bytes(ctypes.byref(p))
+
+
+def mcs_meta_offsets(p: Params) -> tuple[int, int, int]:
+    o = [_sz(0), _sz(0), _sz(0)]
+    _check(lib().mcs_meta_offsets(ctypes.byref(p), *[ctypes.byref(x) for x in o]),
+           "mcs_meta_offsets")
+    return tuple(x.value for x in o)
+
+
+def meta_views(p: Params, entry: torch.Tensor):
+    """(perm, idx, residual) views into a metadata entry (uint8, host or device)."""
+    if entry.dtype != torch.uint8 or not entry.is_contiguous() or entry.dim() != 1:
+        raise ValueError("entry must be a contiguous 1-D uint8 tensor")
+    if entry.numel() < mcs_meta_bytes(p):
+        raise ValueError("entry is smaller than mcs_meta_bytes(p)")
+    po, io, ro = mcs_meta_offsets(p)
+    n_perm = p.B * p.H * p.G * p.C * 4
+    n_idx = p.B * p.H * p.G * p.K * 4
+    n_res = p.B * p.H * p.N * p.D * 2
+    perm = entry[po:po + n_perm].view(torch.int32).view(p.B, p.H, p.G * p.C)
+    idx = entry[io:io + n_idx].view(torch.int32).view(p.B, p.H, p.G, p.K)
+    res = entry[ro:ro + n_res].view(torch.bfloat16).view(p.B, p.H, p.N, p.D)
+    return perm, idx, res
+
+
+class Stager:
+    """Moves metadata entries between host memory and device slots (mcs_stager_*)."""
+
+    def __init__(self, p: Params, slots, copy_stream):
+        for t in slots:
+            _ptr(t, torch.uint8, None, "slot")
+            if t.numel() < mcs_meta_bytes(p):
+                raise ValueError("slot is smaller than mcs_meta_bytes(p)")
+        self.slots = list(slots)
+        self._h = _vp()
+        arr = (_vp * len(slots))(*[t.data_ptr() for t in slots])
+        _check(lib().mcs_stager_create(ctypes.byref(p), len(slots), arr, _stream(copy_stream),
+                                       ctypes.byref(self._h)), "mcs_stager_create")
+
+    @staticmethod
+    def _host(t):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.uint8 or \
+                not t.is_contiguous():
+            raise ValueError("host entry must be a contiguous uint8 CPU tensor (pinned)")
+        return t.data_ptr()
+
+    def prefetch(self, slot: int, host_entry, after=None):
+        _check(lib().mcs_stager_prefetch(self._h, slot, self._host(host_entry), _stream(after)),
+               "mcs_stager_prefetch")
+
+    def offload(self, slot: int, host_entry, after=None):
+        _check(lib().mcs_stager_offload(self._h, slot, self._host(host_entry), _stream(after)),
+               "mcs_stager_offload")
+
+    def wait(self, slot: int, stream=None):
+        _check(lib().mcs_stager_wait(self._h, slot, _stream(stream)), "mcs_stager_wait")
+
+    def close(self):
+        if self._h:
+            lib().mcs_stager_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def empty_workspace(nbytes: int, device="cuda") -> torch.Tensor:
