@@ -28,6 +28,10 @@ the site and the section:
                     kernel).
 * [agihunt/Group]   agihunt.info summary, paragraph on token-level gathering
                     and PDDP groups of exactly C queries.
+* [wisp/Pool]       wispaper.ai, section "Mean-pooled block scoring misses
+                    high-mass tokens".
+* [ai.info/Find]    ai.info AI summary, section "Main Findings" (recall and
+                    relative L1 of the selectors at matched density).
 
 Readings taken where the pages are silent (each repeated at its function):
 softmax scale 1/sqrt(D); natural-log LSE; PDDP centred covariance, power
@@ -65,6 +69,11 @@ __all__ = [
     "sparse_attention_group",
     "anchor_step",
     "reuse_step",
+    "block_topk_select",
+    "pooled_block_select",
+    "per_query_select",
+    "retained_mass",
+    "rel_l1",
 ]
 
 
@@ -349,3 +358,78 @@ def reuse_step(q, k, v, perm, idx, residual, C: int, scale):
     bf16 rounding."""
     sparse = sparse_attention(q, k, v, perm, idx, C, scale)
     return sparse + np.asarray(residual, np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Diagnostic selectors  [wisp/Gap], [ai.info/Method], [wisp/Pool], [ai.info/Find]
+# ---------------------------------------------------------------------------
+# The pages separate the dense-sparse gap by comparing selectors that keep
+# the same number of KV tokens: mean-pooled block-sparse attention (vanilla
+# BSA), a block oracle (whole KV blocks, chosen with the exact probabilities),
+# the token oracle (individual KV tokens shared by a query group: the exact
+# group-mass selection above) and a per-query oracle (every query its own KV
+# tokens).  Readings: KV blocks are the full blocks [b*block, (b+1)*block);
+# the partial block at the end of the sequence (when block does not divide N)
+# is never selected; K must be a multiple of block; ties go to the lower block
+# (or token) index and results are ascending.
+
+def _full_blocks(N: int, K: int, block: int) -> int:
+    if block < 1 or K % block != 0 or K // block > N // block or K < 1:
+        raise ValueError("K must be a positive multiple of block, at most N // block blocks")
+    return N // block
+
+
+def block_topk_select(mass, K: int, block: int):
+    """Block oracle for one group: the K/block full KV blocks of largest
+    summed group mass, expanded to their tokens (ascending).  Returns
+    (idx [K], retained mass)  [wisp/Gap], [ai.info/Method]."""
+    mass = np.asarray(mass, np.float64)
+    nb = _full_blocks(mass.shape[0], K, block)
+    bm = mass[:nb * block].reshape(nb, block).sum(axis=1)
+    order = np.lexsort((np.arange(nb), -bm))
+    blocks = np.sort(order[:K // block])
+    idx = (blocks[:, None] * block + np.arange(block)[None, :]).ravel()
+    return idx, float(mass[idx].sum())
+
+
+def pooled_block_select(q, k, members, K: int, block: int, scale):
+    """Vanilla BSA selection for one query group: each full KV block is
+    scored by the dot product of the group's mean query with the block's mean
+    key (times the softmax scale), and the K/block best blocks are kept,
+    expanded to their tokens (ascending)  [wisp/Pool].  Returns (idx [K],
+    scores [N // block])."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    N, D = k.shape
+    nb = _full_blocks(N, K, block)
+    qbar = q[np.asarray(members)].mean(axis=0)
+    kbar = k[:nb * block].reshape(nb, block, D).mean(axis=1)
+    score = scale * (kbar @ qbar)
+    order = np.lexsort((np.arange(nb), -score))
+    blocks = np.sort(order[:K // block])
+    idx = (blocks[:, None] * block + np.arange(block)[None, :]).ravel()
+    return idx, score
+
+
+def per_query_select(q, k, lse, row: int, K: int, scale):
+    """Per-query oracle for one query: its own K most probable KV tokens
+    (ties to the lower index, ascending) and the probability mass they keep
+    [wisp/Gap], [ai.info/Method].  Equivalent to topk_select on the
+    probabilities of a one-query group."""
+    p = np.exp(scale * (np.asarray(k, np.float64) @ np.asarray(q, np.float64)[row])
+               - float(np.asarray(lse, np.float64)[row]))
+    return topk_select(p, K)
+
+
+def retained_mass(mass, idx) -> float:
+    """Mass a selection keeps: the sum of the group masses at idx.  Divided
+    by the group size it is the group's attention recall [ai.info/Find]."""
+    return float(np.asarray(mass, np.float64)[np.asarray(idx)].sum())
+
+
+def rel_l1(got, want) -> float:
+    """Relative L1 error of an output, sum |got - want| / sum |want|
+    [ai.info/Find]."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    return float(np.abs(got - want).sum() / np.abs(want).sum())

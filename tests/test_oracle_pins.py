@@ -288,3 +288,106 @@ def test_anchor_identity_and_reuse_reproduces_dense():
     sizes = np.array([orc.group_members(a["perm"], g, C).shape[0] for g in range(a["idx"].shape[0])])
     assert np.all(a["retained"] <= sizes + 1e-9)
     np.testing.assert_allclose(a["mass"].sum(1), sizes, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- diagnostic selectors
+
+def test_block_select_with_unit_blocks_is_token_topk():
+    m = _rng(40).random(37)
+    for K in (1, 5, 37):
+        i1, r1 = orc.block_topk_select(m, K, 1)
+        i2, r2 = orc.topk_select(m, K)
+        np.testing.assert_array_equal(i1, i2)
+        assert r1 == pytest.approx(r2, rel=1e-15)
+
+
+@pytest.mark.parametrize("N,block,kb", [(12, 2, 2), (13, 3, 2), (16, 4, 3)])
+def test_block_select_brute_force(N, block, kb):
+    # the chosen blocks maximise the kept mass over every set of kb full
+    # blocks; the partial tail block (13 = 4*3 + 1) is never chosen
+    m = _rng(41 + N).random(N)
+    idx, ret = orc.block_topk_select(m, kb * block, block)
+    nb = N // block
+    best = max(itertools.combinations(range(nb), kb),
+               key=lambda bs: sum(m[b * block:(b + 1) * block].sum() for b in bs))
+    want = np.concatenate([np.arange(b * block, (b + 1) * block) for b in best])
+    np.testing.assert_array_equal(idx, want)
+    assert ret == pytest.approx(m[want].sum(), rel=1e-14)
+    assert idx.max() < nb * block
+
+
+def test_block_select_rejects_budget_not_in_blocks():
+    with pytest.raises(ValueError):
+        orc.block_topk_select(np.ones(10), 3, 2)
+    with pytest.raises(ValueError):
+        orc.block_topk_select(np.ones(10), 12, 2)
+
+
+def test_pooled_block_select_hand_example():
+    # two KV blocks of two keys; the mean query (1, 1) scores block 0
+    # (mean key (1, 0)) at 1 and block 1 (mean key (0.5, 1.5)) at 2
+    q = np.array([[2.0, 0.0], [0.0, 2.0]])
+    k = np.array([[1.0, 1.0], [1.0, -1.0], [0.0, 1.0], [1.0, 2.0]])
+    idx, score = orc.pooled_block_select(q, k, [0, 1], 2, 2, scale=1.0)
+    np.testing.assert_allclose(score, [1.0, 2.0])
+    np.testing.assert_array_equal(idx, [2, 3])
+
+
+def test_pooled_block_select_single_query_unit_blocks_is_per_query_oracle():
+    # one query, blocks of one key: the pooled score is the query's own
+    # score, whose order is its probability order
+    rng = _rng(43)
+    q = _bf16(rng.standard_normal((5, 16)))
+    k = _bf16(rng.standard_normal((40, 16)))
+    scale = orc.default_scale(16)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    for row in range(5):
+        idx, _ = orc.pooled_block_select(q, k, [row], 9, 1, scale)
+        want, _ = orc.per_query_select(q, k, lse, row, 9, scale)
+        np.testing.assert_array_equal(idx, want)
+
+
+def test_per_query_select_matches_per_query_topk_mass_and_sdpa_probabilities():
+    rng = _rng(44)
+    q = _bf16(rng.standard_normal((6, 32)))
+    k = _bf16(rng.standard_normal((50, 32)))
+    scale = orc.default_scale(32)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    P = torch.softmax(torch.from_numpy(q) @ torch.from_numpy(k).T * scale, dim=-1).numpy()
+    masses = orc.per_query_topk_mass(q, k, lse, np.arange(6), 12, scale)
+    for row in range(6):
+        idx, ret = orc.per_query_select(q, k, lse, row, 12, scale)
+        want = np.sort(np.argsort(-P[row], kind="stable")[:12])
+        np.testing.assert_array_equal(idx, want)
+        assert ret == pytest.approx(masses[row], rel=1e-12)
+
+
+def test_recall_ordering_per_query_token_block():
+    # at the same number of kept tokens: the per-query optimum keeps at least
+    # what the group's token optimum keeps (summed over the group), which
+    # keeps at least what the best whole blocks keep; all reach the group
+    # size when every token is kept
+    rng = _rng(45)
+    N, D, C, block = 64, 16, 8, 4
+    q = _bf16(rng.standard_normal((N, D)))
+    k = _bf16(rng.standard_normal((N, D)))
+    scale = orc.default_scale(D)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    members = np.arange(8, 16)
+    mass = orc.group_mass(q, k, lse, members, scale)
+    for K in (8, 16, 32, 64):
+        pq = orc.per_query_topk_mass(q, k, lse, members, K, scale).sum()
+        _, tok = orc.topk_select(mass, K)
+        _, blk = orc.block_topk_select(mass, K, block)
+        pidx, _ = orc.pooled_block_select(q, k, members, K, block, scale)
+        pooled = orc.retained_mass(mass, pidx)
+        assert pq >= tok - 1e-12 >= blk - 2e-12 >= pooled - 3e-12
+    assert tok == pytest.approx(C, rel=1e-12) and blk == pytest.approx(C, rel=1e-12)
+
+
+def test_rel_l1_closed_forms():
+    w = _rng(46).standard_normal((7, 3))
+    assert orc.rel_l1(w, w) == 0.0
+    assert orc.rel_l1(2 * w, w) == pytest.approx(1.0)
+    assert orc.rel_l1(np.zeros_like(w), w) == pytest.approx(1.0)
+    assert orc.rel_l1(w + 0.5, w) == pytest.approx(0.5 * w.size / np.abs(w).sum())
