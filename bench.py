@@ -459,6 +459,98 @@ def run_gpu(args, w, K, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_diagnostics(args, w):
+    """Selector diagnostics: attention recall and output relative L1 of
+    mean-pooled block selection, the block oracle, the token oracle (exact
+    group mass) and the per-query oracle, at matched numbers of kept tokens,
+    under raster (consecutive tiles) and PDDP query groups.  One JSON line."""
+    from token_sparse_attention_gb300 import mcs
+
+    mcs.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    block = 128
+    H = w.H
+    q, k, v = synth.make_qkv(w, 0, device=dev)
+    G = -(-w.N // w.C)
+    p0 = mcs.params(w.B, H, w.N, w.D, w.C, w.N)
+    dense = torch.empty_like(q)
+    lse = torch.empty(w.B, H, w.N, dtype=torch.float32, device=dev)
+    mcs.mcs_dense_attn(p0, q, k, v, dense, lse)
+    raster = torch.arange(G * w.C, dtype=torch.int32, device=dev)
+    raster[w.N:] = -1
+    groupings = {"raster": raster.expand(w.B, H, -1).contiguous()}
+    pddp = torch.empty(w.B, H, G * w.C, dtype=torch.int32, device=dev)
+    mcs.mcs_group(p0, q, pddp, mcs.empty_workspace(mcs.mcs_group_workspace(p0), dev))
+    groupings["pddp"] = pddp
+    # per-query oracle: G sampled queries per head, each alone in a group
+    gen = torch.Generator().manual_seed(99)
+    sample = torch.stack([torch.randperm(w.N, generator=gen)[:G].sort().values for _ in range(H)])
+    one = torch.full((w.B, H, G * w.C), -1, dtype=torch.int32)
+    one[..., ::w.C] = sample.to(torch.int32)
+    one = one.to(dev)
+    sample_rows = (torch.arange(H)[:, None] * w.N + sample).reshape(-1).to(torch.int32).to(dev)
+    BH = w.B * H
+    rows = []
+    timings = {}
+
+    def timed(name, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        timings.setdefault(name, []).append(a.elapsed_time(b))
+
+    masses = {}
+    for name, perm in list(groupings.items()) + [("one-query", one)]:
+        m = torch.empty(BH, G, w.N, dtype=torch.float32, device=dev)
+        timed("group_mass", lambda: mcs.mcs_group_mass(p0, q, k, lse, perm, 0, BH, m))
+        masses[name] = m
+    sizes = torch.tensor([min(w.C, w.N - g * w.C) for g in range(G)], dtype=torch.float64)
+    for s_ in (0.1, 0.2, 0.3):
+        K = max(block, round(s_ * w.N / block) * block)
+        p = mcs.params(w.B, H, w.N, w.D, w.C, K)
+        ws = mcs.empty_workspace(mcs.mcs_block_workspace(p, block), dev)
+        out = torch.empty_like(q)
+
+        def record(grouping, selector, idx, kept, rows_sel=None, denom=None):
+            perm = one if grouping == "one-query" else groupings[grouping]
+            mcs.mcs_sparse_attn(p, q, k, v, perm, idx, None, out)
+            e, d = mcs.mcs_rel_l1(p, out, dense, rows_sel)
+            # attention recall: kept probability mass per query, averaged over queries
+            recall = float(kept.double().sum().cpu() / (denom.sum() * BH))
+            rows.append({"density": K / w.N, "K": K, "grouping": grouping, "selector": selector,
+                         "recall": recall, "rel_l1": e / d})
+
+        for gname, perm in groupings.items():
+            mass = masses[gname]
+            idx = torch.empty(w.B, H, G, K, dtype=torch.int32, device=dev)
+            kept = torch.empty(BH * G, dtype=torch.float32, device=dev)
+            timed("pooled_block_select", lambda: mcs.mcs_pooled_block_select(p, q, k, perm, block,
+                                                                            idx, ws))
+            timed("gather_mass", lambda: mcs.mcs_gather_mass(p, mass, idx, kept))
+            record(gname, f"mean-pooled blocks of {block}", idx, kept, denom=sizes)
+            timed("block_topk", lambda: mcs.mcs_block_topk(p, mass, block, idx, ws, retained=kept))
+            record(gname, f"block oracle ({block})", idx, kept, denom=sizes)
+            timed("topk", lambda: mcs.mcs_topk(p, mass, idx, kept))
+            record(gname, "token oracle", idx, kept, denom=sizes)
+        idx = torch.empty(w.B, H, G, K, dtype=torch.int32, device=dev)
+        kept = torch.empty(BH * G, dtype=torch.float32, device=dev)
+        mcs.mcs_topk(p, masses["one-query"], idx, kept)
+        record("one-query", "per-query oracle (sampled queries)", idx, kept, sample_rows,
+               denom=torch.ones(G, dtype=torch.float64))
+    if mcs.mcs_device_status() != 0:
+        raise RuntimeError("device status after the diagnostics")
+    print(json.dumps({
+        "diagnostics": "selector recall and output relative L1 (sparse output without the "
+                       "residual against dense attention), matched numbers of kept tokens",
+        "workload": f"{w.name} B={w.B} H={H} N={w.N} D={w.D} C={w.C}", "data": "synthetic",
+        "block": block, "per_query_sample": f"{G} random queries per head (seed 99)",
+        "rows": rows,
+        "kernel_ms": {n: statistics.median(t) for n, t in timings.items()},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,6 +561,8 @@ def main():
     ap.add_argument("--density", type=float, default=0.2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--diagnostics", action="store_true",
+                    help="print the selector diagnostics line instead of the bench line")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (smaller cases for profiling; not a bench number)")
     args = ap.parse_args()
@@ -486,6 +580,9 @@ def main():
         return
 
     torch.cuda.set_device(local)
+    if args.diagnostics:
+        run_diagnostics(args, w)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist_mod

@@ -267,6 +267,56 @@ mcs_status mcs_stager_offload(mcs_stager* s, int slot, void* host_entry, cudaStr
 /* Makes `stream` wait (on the device) for the slot's last queued copy. */
 mcs_status mcs_stager_wait(mcs_stager* s, int slot, cudaStream_t stream);
 
+/*
+ * Diagnostic selectors and error measures.  The pages separate the
+ * dense-sparse gap by comparing, at the same number of kept KV tokens,
+ * mean-pooled block-sparse attention, a block oracle, the token oracle
+ * (mcs_select) and a per-query oracle (a group of one query: mcs_group_mass +
+ * mcs_topk on a perm with one query per group), by attention recall and by
+ * the relative L1 error of the output (wispaper.ai, "The gap has three
+ * separable sources"; wispaper.ai, "Mean-pooled block scoring misses
+ * high-mass tokens"; ai.info AI summary, "Main Findings").
+ *
+ * KV blocks are the full blocks [b*block, (b+1)*block), b < N / block; the
+ * partial block at the end is never selected.  K (p->K) must be a multiple of
+ * block with K / block <= N / block, 1 <= block <= 1024.  Selected token
+ * indices are ascending; ties go to the lower block.
+ */
+/* Workspace bytes of mcs_block_topk and mcs_pooled_block_select (all groups). */
+size_t mcs_block_workspace(const mcs_params* p, int block);
+
+/*
+ * Block oracle: for each of `rows` rows of N group masses (as from
+ * mcs_group_mass), keeps the K / block full KV blocks of largest summed mass;
+ * idx [rows, K] (tokens of the kept blocks), retained [rows] (their mass,
+ * nullable).  rows <= B*H*G.
+ */
+mcs_status mcs_block_topk(const mcs_params* p, const float* mass, int rows, int block,
+                          int32_t* idx, float* retained, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/*
+ * Mean-pooled block-sparse selection: each group (perm) scores each full KV
+ * block by scale * (mean of its query rows) . (mean of the block's key rows),
+ * in fp32, and keeps the K / block best; idx [B,H,G,K].
+ */
+mcs_status mcs_pooled_block_select(const mcs_params* p, const void* q, const void* k,
+                                   const int32_t* perm, int block, int32_t* idx, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream);
+
+/* retained[r] = sum_t mass[r, idx[r, t]] for rows of N masses and K indices. */
+mcs_status mcs_gather_mass(const mcs_params* p, const float* mass, int rows, const int32_t* idx,
+                           float* retained, cudaStream_t stream);
+
+/*
+ * Relative L1 terms of an output: sums[0] = sum |got - want|, sums[1] =
+ * sum |want| (device doubles, overwritten) over the D values of each row
+ * listed in rows [nrows] (indices into the B*H*N rows of [B,H,N,D] bf16
+ * tensors), or over every row when rows is NULL.
+ */
+mcs_status mcs_rel_l1(const mcs_params* p, const void* got, const void* want, const int32_t* rows,
+                      int nrows, double* sums, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ def L():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "mcs.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mcs_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mcs_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_binding_names():

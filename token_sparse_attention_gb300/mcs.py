@@ -22,7 +22,8 @@ __all__ = [
     "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
     "mcs_group_mass", "mcs_topk", "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record",
     "mcs_anchor_select", "mcs_group_noalloc", "mcs_meta_bytes", "mcs_meta_offsets",
-    "meta_views", "Stager",
+    "meta_views", "Stager", "mcs_block_workspace", "mcs_block_topk", "mcs_pooled_block_select",
+    "mcs_gather_mass", "mcs_rel_l1",
 ]
 
 # Every symbol include/mcs.h declares.
@@ -31,7 +32,8 @@ EXPORTED = (
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
     "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
     "mcs_meta_bytes", "mcs_meta_offsets", "mcs_stager_create", "mcs_stager_destroy",
-    "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait",
+    "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait", "mcs_block_workspace",
+    "mcs_block_topk", "mcs_pooled_block_select", "mcs_gather_mass", "mcs_rel_l1",
 )
 
 STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
@@ -92,6 +94,11 @@ _SIGS = {
     "mcs_stager_prefetch": ([_vp, _i, _vp, _vp], _st),
     "mcs_stager_offload": ([_vp, _i, _vp, _vp], _st),
     "mcs_stager_wait": ([_vp, _i, _vp], _st),
+    "mcs_block_workspace": ([_pp, _i], _sz),
+    "mcs_block_topk": ([_pp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp], _st),
+    "mcs_pooled_block_select": ([_pp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp], _st),
+    "mcs_gather_mass": ([_pp, _vp, _i, _vp, _vp, _vp], _st),
+    "mcs_rel_l1": ([_pp, _vp, _vp, _vp, _i, _vp, _vp], _st),
 }
 
 
@@ -326,6 +333,54 @@ class Stager:
             self.close()
         except Exception:
             pass
+
+
+def mcs_block_workspace(p: Params, block: int) -> int:
+    return lib().mcs_block_workspace(ctypes.byref(p), block)
+
+
+def mcs_block_topk(p: Params, mass, block: int, idx, ws, retained=None, stream=None):
+    rows = mass.numel() // p.N
+    _ptr(idx, torch.int32, None, "idx")
+    if idx.numel() != rows * p.K:
+        raise ValueError("idx must hold rows * K entries")
+    _check(lib().mcs_block_topk(ctypes.byref(p), _ptr(mass, torch.float32, None, "mass"), rows,
+                                block, idx.data_ptr(),
+                                _ptr(retained, torch.float32, (rows,), "retained", optional=True),
+                                _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)),
+           "mcs_block_topk")
+
+
+def mcs_pooled_block_select(p: Params, q, k, perm, block: int, idx, ws, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_pooled_block_select(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"), block,
+        _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)), "mcs_pooled_block_select")
+
+
+def mcs_gather_mass(p: Params, mass, idx, retained, stream=None):
+    rows = mass.numel() // p.N
+    _ptr(idx, torch.int32, None, "idx")
+    if idx.numel() != rows * p.K:
+        raise ValueError("idx must hold rows * K entries")
+    _check(lib().mcs_gather_mass(ctypes.byref(p), _ptr(mass, torch.float32, None, "mass"), rows,
+                                 idx.data_ptr(), _ptr(retained, torch.float32, (rows,), "retained"),
+                                 _stream(stream)), "mcs_gather_mass")
+
+
+def mcs_rel_l1(p: Params, got, want, rows=None, stream=None) -> tuple:
+    """(sum |got - want|, sum |want|) over the listed rows (all when None);
+    synchronises the stream to read the two sums."""
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    sums = torch.empty(2, dtype=torch.float64, device=got.device)
+    nrows = 0 if rows is None else rows.numel()
+    _check(lib().mcs_rel_l1(ctypes.byref(p), _ptr(got, bf, s, "got"), _ptr(want, bf, s, "want"),
+                            _ptr(rows, torch.int32, None, "rows", optional=True), nrows,
+                            sums.data_ptr(), _stream(stream)), "mcs_rel_l1")
+    v = sums.cpu()
+    return float(v[0]), float(v[1])
 
 
 def empty_workspace(nbytes: int, device="cuda") -> torch.Tensor:
