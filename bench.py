@@ -228,11 +228,16 @@ def run_gpu(args, w, K, rank, world, dist):
 
     mcs.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
-    p = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
+    layout = mcs.LAYOUT_BNHD if args.layout == "bnhd" else mcs.LAYOUT_BHND
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, K, layout=layout)
     G = p.G
     BH = w.B * w.H
-    q0, k0, v0 = synth.make_qkv(w, 0, device=dev)
-    q1, k1, v1 = synth.make_qkv(w, 1, device=dev)
+
+    def lay(t):  # the generator writes [B,H,N,D]; DiT blocks hold [B,N,H,D]
+        return t.transpose(1, 2).contiguous() if layout == mcs.LAYOUT_BNHD else t
+
+    q0, k0, v0 = (lay(t) for t in synth.make_qkv(w, 0, device=dev))
+    q1, k1, v1 = (lay(t) for t in synth.make_qkv(w, 1, device=dev))
     perm = torch.empty(w.B, w.H, G * w.C, dtype=torch.int32, device=dev)
     idx = torch.empty(w.B, w.H, G, K, dtype=torch.int32, device=dev)
     dense = torch.empty_like(q0)
@@ -428,6 +433,7 @@ def run_gpu(args, w, K, rank, world, dist):
             "value_basis": "reuse-step sparse attention kernel time, CUDA events, mean of timed steps",
             "l2": "inputs larger than L2 (0.77 GB per tensor); no flush",
             "parallelism": f"dp{world} (independent replicas)",
+            "layout": "[B,N,H,D]" if layout == mcs.LAYOUT_BNHD else "[B,H,N,D]",
         },
         "speedup_vs_dense": speedup,
         "efficiency_vs_ideal": speedup * args.density,
@@ -561,6 +567,8 @@ def main():
     ap.add_argument("--density", type=float, default=0.2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"],
+                    help="activation layout: [B,H,N,D] or [B,N,H,D]")
     ap.add_argument("--diagnostics", action="store_true",
                     help="print the selector diagnostics line instead of the bench line")
     ap.add_argument("--heads", type=int, default=0,

@@ -11,7 +11,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Tensors are caller-owned DEVICE memory, contiguous, row-major:
- *      q, k, v, out, dense_out, residual : [B, H, N, D] bfloat16
+ *      q, k, v, out, dense_out, residual : [B, H, N, D] bfloat16, or
+ *                                          [B, N, H, D] when p->layout is
+ *                                          MCS_LAYOUT_BNHD (as DiT blocks
+ *                                          hold them); results are identical
  *      lse                               : [B, H, N]    float32 (natural log)
  *      perm                              : [B, H, G*C]  int32, G = ceil(N/C)
  *      idx                               : [B, H, G, K] int32
@@ -61,7 +64,11 @@ typedef struct {
   int K;           /* selected KV tokens per group: round(density * N) */
   float scale;     /* softmax scale; 0 selects 1/sqrt(D) */
   int pddp_iters;  /* power-iteration steps per PDDP node; 0 selects 32 */
+  int layout;      /* MCS_LAYOUT_BHND (0) or MCS_LAYOUT_BNHD (1): see below */
 } mcs_params;
+
+/* Layout of the bf16 activations q, k, v, out, dense_out and residual. */
+enum { MCS_LAYOUT_BHND = 0, MCS_LAYOUT_BNHD = 1 };
 
 /* Human-readable name of a status code (static string). */
 const char* mcs_status_string(mcs_status s);
@@ -311,8 +318,9 @@ mcs_status mcs_gather_mass(const mcs_params* p, const float* mass, int rows, con
 /*
  * Relative L1 terms of an output: sums[0] = sum |got - want|, sums[1] =
  * sum |want| (device doubles, overwritten) over the D values of each row
- * listed in rows [nrows] (indices into the B*H*N rows of [B,H,N,D] bf16
- * tensors), or over every row when rows is NULL.
+ * listed in rows [nrows] (indices of D-vectors in memory order: rows of the
+ * bf16 tensors viewed as [B*H*N, D], in their layout), or over every row when
+ * rows is NULL.
  */
 mcs_status mcs_rel_l1(const mcs_params* p, const void* got, const void* want, const int32_t* rows,
                       int nrows, double* sums, cudaStream_t stream);

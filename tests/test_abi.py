@@ -122,3 +122,13 @@ def test_stager_rejects_bad_arguments(L):
     assert L.mcs_stager_offload(None, 0, 16, None) == 1
     assert L.mcs_stager_wait(None, 0, None) == 1
     L.mcs_stager_destroy(None)
+
+
+def test_layout_field_is_checked_on_the_host(L):
+    # layout 0 ([B,H,N,D]) and 1 ([B,N,H,D]) are accepted; anything else is
+    # an invalid argument, reported before any CUDA call
+    for layout, want in ((2, 1), (-1, 1)):
+        p = mcs.params(1, 2, 256, 128, 64, 40, layout=layout)
+        assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 16, 16, None, None) == want
+        assert L.mcs_meta_bytes(ctypes.byref(p)) == 0
+    assert ctypes.sizeof(mcs.Params) == 9 * 4

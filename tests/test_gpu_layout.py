@@ -1,0 +1,88 @@
+"""[B,N,H,D] activations (the layout DiT blocks hold) give bit-identical
+results to [B,H,N,D] through every entry point that reads or writes them:
+only addresses change, never the arithmetic.  Every call goes through the C
+ABI (libmcs.so)."""
+
+import numpy as np
+import pytest
+import torch
+
+from tests import parity as P
+from token_sparse_attention_gb300 import build as mcs_build
+from token_sparse_attention_gb300 import mcs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mcs_build.build()
+    mcs.lib()
+    assert torch.cuda.is_available()
+    yield
+    assert mcs.mcs_device_status() == 0
+
+
+def bnhd(t):
+    return t.transpose(1, 2).contiguous()
+
+
+def same(a, b, what):
+    assert torch.equal(a.cpu(), b.cpu()), what
+
+
+CASES = [(2, 3, 1000, 128, 128, 300), (1, 2, 777, 64, 64, 200), (2, 2, 300, 128, 64, 300)]
+
+
+@pytest.mark.parametrize("B,H,N,D,C,K", CASES)
+def test_anchor_and_reuse_are_layout_independent(B, H, N, D, C, K):
+    q, k, v = [t.cuda() for t in P.random_qkv(B, H, N, D, seed=N + D)]
+    q1, k1, v1 = [t.cuda() for t in P.random_qkv(B, H, N, D, seed=N + D + 1)]
+    res = {}
+    for layout in (mcs.LAYOUT_BHND, mcs.LAYOUT_BNHD):
+        p = mcs.params(B, H, N, D, C, K, layout=layout)
+        cv = bnhd if layout == mcs.LAYOUT_BNHD else (lambda t: t)
+        back = bnhd if layout == mcs.LAYOUT_BNHD else (lambda t: t)
+        qa, ka, va = cv(q), cv(k), cv(v)
+        perm = torch.empty(B, H, p.G * C, dtype=torch.int32, device="cuda")
+        idx = torch.empty(B, H, p.G, K, dtype=torch.int32, device="cuda")
+        dense, resid = torch.empty_like(qa), torch.empty_like(qa)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+        ret = torch.empty(B, H, p.G, dtype=torch.float32, device="cuda")
+        ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
+        mcs.mcs_anchor_select(p, qa, ka, va, perm, idx, dense, lse, resid, ws, retained=ret)
+        out = torch.empty_like(qa)
+        mcs.mcs_sparse_attn(p, cv(q1), cv(k1), cv(v1), perm, idx, resid, out)
+        # the entry points one at a time
+        perm2 = torch.empty_like(perm)
+        mcs.mcs_group(p, qa, perm2, mcs.empty_workspace(mcs.mcs_group_workspace(p)))
+        perm3 = torch.empty_like(perm)
+        mcs.mcs_group_noalloc(p, qa, perm3)
+        mass = torch.empty(B * H, p.G, N, dtype=torch.float32, device="cuda")
+        mcs.mcs_group_mass(p, qa, ka, lse, perm, 0, B * H, mass)
+        rec = torch.empty_like(qa)
+        mcs.mcs_sparse_attn_record(p, qa, ka, va, perm, idx, dense, rec)
+        plain = torch.empty_like(qa)
+        mcs.mcs_sparse_attn(p, qa, ka, va, perm, idx, None, plain)
+        blk = 16 if K % 16 == 0 else 1
+        pb = mcs.params(B, H, N, D, C, (K // blk) * blk, layout=layout)
+        pidx = torch.empty(B, H, p.G, pb.K, dtype=torch.int32, device="cuda")
+        mcs.mcs_pooled_block_select(pb, qa, ka, perm, blk, pidx,
+                                    mcs.empty_workspace(mcs.mcs_block_workspace(pb, blk)))
+        assert mcs.mcs_device_status() == 0
+        res[layout] = dict(perm=perm, idx=idx, dense=back(dense), lse=lse, resid=back(resid),
+                           ret=ret, out=back(out), perm2=perm2, perm3=perm3, mass=mass,
+                           rec=back(rec), plain=back(plain), pidx=pidx)
+    a, b = res[mcs.LAYOUT_BHND], res[mcs.LAYOUT_BNHD]
+    for name in a:
+        same(a[name], b[name], name)
+    # sanity: the anchor produced groups and a residual that reproduces dense
+    P.check_valid_perm(a["perm"][0, 0].cpu().numpy(), N, C)
+    assert np.isfinite(P.f64(a["dense"])).all()
+
+
+def test_bad_layout_is_rejected_before_launch():
+    p = mcs.params(1, 1, 256, 128, 64, 40, layout=2)
+    q = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mcs.McsError):
+        mcs.mcs_dense_attn(p, q, q, q, torch.empty_like(q))

@@ -141,6 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = lane_id();
   const int pair = blockIdx.x;
   const int bh = blockIdx.y;
+  const int head_h = bh % a.H, head_b = bh / a.H;    // tile-map coordinates of this head
+  const RowMap rm = row_map(a.layout, a.H, a.N, bh);  // rows of q/k/v/out in either layout
   const int units = kSparseMode ? a.G : (a.N + BM - 1) / BM;  // units per head
   const bool has_b = 2 * pair + 1 < units;
   const int kv_total = kSparseMode ? a.K : a.N;
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(q_full, 2 * L::kTileBytes);
           for (int x = 0; x < 2; ++x)
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(qs + x * L::kTileBytes + s * L::kSubBytes, &tq, s * 64,
-                          (2 * pair + x) * BM, bh, q_full);
+              tma_load_4d(qs + x * L::kTileBytes + s * L::kSubBytes, &tq, s * 64,
+                          (2 * pair + x) * BM, head_h, head_b, q_full);
         }
         __syncwarp();
         for (int i = 0; i < 2 * nkv; ++i) {
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* tm = (i & 1) ? &tv : &tk;
             uint8_t* dst = ring + st * L::kTileBytes;
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, bh, full + st);
+              tma_load_4d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, head_h, head_b,
+                          full + st);
           }
           ++issued;
         }
@@ -243,13 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tok = (r < a.C && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
             if (tok >= a.N) { bad = true; tok = -1; }
             const __nv_bfloat16* src =
-                a.q + (static_cast<size_t>(bh) * a.N + (tok < 0 ? 0 : tok)) * D + seg * 8;
+                a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + seg * 8;
             cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, seg), src, tok >= 0);
           }
         }
       }
       cp_async_arrive(q_full);
-      // Global rows (b*H+h)*N + token of this thread's chunks of tile j of
+      // Rows (RowMap) of the tokens of this thread's chunks of tile j of
       // unit x; loaded two tiles ahead so that the index latency (the index
       // array is read once, from HBM) stays off the critical path.
       auto load_rows = [&](int x, int j, int* out) {
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked in softmax
           int tok = __ldg(idx_g + col);
           if (tok < 0 || tok >= a.N) { bad = true; tok = 0; }
-          out[k] = bh * a.N + tok;
+          out[k] = rm.rbase + tok * rm.rstride;
         }
       };
       // Copy the rows of one K or V tile into the stage of ring item `it`.
@@ -518,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     : -1;
         if (token >= a.N) token = -1;
       }
-      const size_t row_off = (static_cast<size_t>(bh) * a.N + (token < 0 ? 0 : token)) * D;
+      const size_t row_off =
+          static_cast<size_t>(rm.rbase + (token < 0 ? 0 : token) * rm.rstride) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

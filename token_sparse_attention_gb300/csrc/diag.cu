@@ -58,8 +58,9 @@ __global__ void expand_blocks_kernel(const int32_t* __restrict__ bidx, int kb, i
 // One CTA of D threads per (group, head).
 __global__ void pool_queries_kernel(const __nv_bfloat16* __restrict__ q,
                                     const int32_t* __restrict__ perm, int N, int D, int C, int G,
-                                    float* __restrict__ qbar, unsigned* status) {
+                                    int layout, int H, float* __restrict__ qbar, unsigned* status) {
   const int g = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const RowMap rm = row_map(layout, H, N, bh);
   const int32_t* pg = perm + (static_cast<size_t>(bh) * G + g) * C;
   float s = 0.f;
   int cnt = 0;
@@ -70,7 +71,7 @@ __global__ void pool_queries_kernel(const __nv_bfloat16* __restrict__ q,
       if (d == 0) atomicOr(status, DEV_BOUNDS);
       continue;
     }
-    s += __bfloat162float(q[(static_cast<size_t>(bh) * N + t) * D + d]);
+    s += __bfloat162float(q[static_cast<size_t>(rm.rbase + t * rm.rstride) * D + d]);
     ++cnt;
   }
   qbar[(static_cast<size_t>(bh) * G + g) * D + d] = cnt > 0 ? s / cnt : 0.f;
@@ -79,11 +80,12 @@ __global__ void pool_queries_kernel(const __nv_bfloat16* __restrict__ q,
 // kbar[bh, b, :] = mean of the key rows of full block b.  One CTA of D
 // threads per (block, head).
 __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k, int N, int D, int block,
-                                 int nb, float* __restrict__ kbar) {
+                                 int nb, int layout, int H, float* __restrict__ kbar) {
   const int b = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
-  const __nv_bfloat16* src = k + (static_cast<size_t>(bh) * N + static_cast<size_t>(b) * block) * D;
+  const RowMap rm = row_map(layout, H, N, bh);
   float s = 0.f;
-  for (int t = 0; t < block; ++t) s += __bfloat162float(src[static_cast<size_t>(t) * D + d]);
+  for (int t = b * block; t < (b + 1) * block; ++t)
+    s += __bfloat162float(k[static_cast<size_t>(rm.rbase + t * rm.rstride) * D + d]);
   kbar[(static_cast<size_t>(bh) * nb + b) * D + d] = s / block;
 }
 
@@ -300,9 +302,10 @@ mcs_status mcs_pooled_block_select(const mcs_params* p, const void* q, const voi
   const float scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* kbf = static_cast<const __nv_bfloat16*>(k);
-  mcs::pool_queries_kernel<<<dim3(G, BH), p->D, 0, stream>>>(qb, perm, p->N, p->D, p->C, G, qbar,
-                                                             st);
-  mcs::pool_keys_kernel<<<dim3(nb, BH), p->D, 0, stream>>>(kbf, p->N, p->D, block, nb, kbar);
+  mcs::pool_queries_kernel<<<dim3(G, BH), p->D, 0, stream>>>(qb, perm, p->N, p->D, p->C, G,
+                                                             p->layout, p->H, qbar, st);
+  mcs::pool_keys_kernel<<<dim3(nb, BH), p->D, 0, stream>>>(kbf, p->N, p->D, block, nb, p->layout,
+                                                           p->H, kbar);
   mcs::pooled_scores_kernel<<<dim3(G, BH), 256, 0, stream>>>(qbar, kbar, p->D, G, nb, scale,
                                                              keys);
   e = cudaGetLastError();

@@ -23,6 +23,24 @@ enum : unsigned {
   DEV_BOUNDS = 2u,   // an index read from an argument was out of range
 };
 
+// Rows of the [B,H,N,D] (layout 0) or [B,N,H,D] (layout 1) bf16 tensors q, k,
+// v, out, dense_out and residual, viewed as [B*H*N, D]: the vector of head
+// bh = b*H + h at token t is row rbase + t * rstride.
+struct RowMap {
+  int rbase, rstride;
+};
+__host__ __device__ __forceinline__ RowMap row_map(int layout, int H, int N, int bh) {
+  RowMap m;
+  if (layout == 1) {
+    m.rbase = (bh / H) * N * H + bh % H;
+    m.rstride = H;
+  } else {
+    m.rbase = bh * N;
+    m.rstride = 1;
+  }
+  return m;
+}
+
 // Attention kernel modes.
 enum AttnMode : int {
   kDense = 0,         // dense attention, writes O (+ LSE)
@@ -32,6 +50,7 @@ enum AttnMode : int {
 };
 
 struct AttnArgs {
+  int H, layout;     // heads per batch entry; tensor layout (see RowMap)
   int N;             // tokens per head
   int C;             // queries per group (sparse modes)
   int G;             // groups per head (sparse modes)
@@ -49,13 +68,15 @@ struct AttnArgs {
   int fault;                     // test-only: 1 = producers stop after the first K/V tile
 };
 
-// tq/tk/tv: dense -> 3-D tile maps [BH][N][D], box {64,128,1};
-//           sparse -> 2-D gather maps [BH*N][D], box {64,1}.
+// tq/tk/tv: dense -> 4-D tile maps [B][H][N][D] in the tensors' layout, box
+//           {64,128,1,1}, coordinates (d, token, h, b);
+//           sparse -> 2-D gather maps [B*H*N rows][D], box {64,1}.
 cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUtensorMap* tk,
                              const CUtensorMap* tv, const AttnArgs& a, int BH,
                              cudaStream_t stream);
 
 struct MassArgs {
+  int H, layout;          // heads per batch entry; tensor layout (see RowMap)
   int N, C, G;
   int head0;              // first (b*H+h) head of this chunk
   float scale_log2;
@@ -66,7 +87,7 @@ struct MassArgs {
   unsigned* status;
 };
 
-// tq: 2-D gather map over Q [BH*N][D]; tk: 3-D tile map over K.
+// tq: 2-D gather map over the rows of Q; tk: 4-D tile map over K.
 cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* tk,
                               const MassArgs& a, int heads, cudaStream_t stream);
 
@@ -82,8 +103,11 @@ cudaError_t device_status_word(unsigned** out);
 bool encode_gather_map(CUtensorMap* m, const void* base, long long rows, int D);
 
 size_t pddp_workspace_bytes(int BH, int N, int D, int C);
-cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int BH, int N, int D,
-                        int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,
-                        unsigned* status, cudaStream_t stream);
+// Groups heads [head0, head0 + BH) of q (all B*H heads, in `layout`, H heads
+// per batch entry); tq_gather covers every row of q.  perm_out points at the
+// first of those heads' perm rows.
+cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int layout, int H,
+                        int head0, int BH, int N, int D, int C, int iters, int32_t* perm_out,
+                        void* ws, size_t ws_bytes, unsigned* status, cudaStream_t stream);
 
 }  // namespace mcs

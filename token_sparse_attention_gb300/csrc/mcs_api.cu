@@ -42,16 +42,26 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [BH][N][D] bf16 viewed as 3-D, box {64, 128, 1}: 128-row tiles of one head,
-// rows past N zero-filled.
-bool make_tile_map(CUtensorMap* m, const void* base, int BH, int N, int D) {
+// A q/k/v-shaped bf16 tensor viewed as 4-D (d, token, h, b) whatever its
+// layout ([B,H,N,D] or [B,N,H,D]: only the strides differ), box
+// {64, 128, 1, 1}: 128-token tiles of one head, tokens past N zero-filled.
+bool make_tile_map(CUtensorMap* m, const void* base, const mcs_params* p) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  const cuuint64_t D = p->D, N = p->N, H = p->H, row = D * 2;
+  cuuint64_t dims[4] = {D, N, H, (cuuint64_t)p->B};
+  cuuint64_t strides[3];
+  if (p->layout == MCS_LAYOUT_BNHD) {
+    strides[0] = H * row;      // token
+    strides[1] = row;          // head
+  } else {
+    strides[0] = row;
+    strides[1] = N * row;
+  }
+  strides[2] = N * H * row;    // batch
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -81,6 +91,7 @@ mcs_status check_shape(const mcs_params* p, bool need_k) {
   if (need_k && (p->K < 1 || p->K > p->N)) return MCS_ERR_INVALID_ARG;
   if (p->scale < 0.f || !isfinite(p->scale)) return MCS_ERR_INVALID_ARG;
   if (p->pddp_iters < 0) return MCS_ERR_INVALID_ARG;
+  if (p->layout != MCS_LAYOUT_BHND && p->layout != MCS_LAYOUT_BNHD) return MCS_ERR_INVALID_ARG;
   return MCS_OK;
 }
 
@@ -123,6 +134,8 @@ mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const v
       !make_gather_map(&tv, v, BH, p->N, p->D))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(gather)");
   mcs::AttnArgs a{};
+  a.H = p->H;
+  a.layout = p->layout;
   a.N = p->N;
   a.C = p->C;
   a.G = groups_of(p);
@@ -165,9 +178,11 @@ mcs_status run_group_mass(const mcs_params* p, const void* q, const void* k, con
                           cudaStream_t stream) {
   const int BH = p->B * p->H;
   CUtensorMap tq, tk;
-  if (!make_gather_map(&tq, q, BH, p->N, p->D) || !make_tile_map(&tk, k, BH, p->N, p->D))
+  if (!make_gather_map(&tq, q, BH, p->N, p->D) || !make_tile_map(&tk, k, p))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(mass)");
   mcs::MassArgs a{};
+  a.H = p->H;
+  a.layout = p->layout;
   a.N = p->N;
   a.C = p->C;
   a.G = groups_of(p);
@@ -269,7 +284,8 @@ mcs_status mcs_group(const mcs_params* p, const void* q, int32_t* perm, void* ws
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(gather)");
   unsigned* st;
   if ((s = status_ptr(&st)) != MCS_OK) return s;
-  cudaError_t e = mcs::launch_pddp(static_cast<const __nv_bfloat16*>(q), &tq, BH, p->N, p->D, p->C,
+  cudaError_t e = mcs::launch_pddp(static_cast<const __nv_bfloat16*>(q), &tq, p->layout, p->H, 0, BH,
+                                   p->N, p->D, p->C,
                                    iters_of(p), perm, ws, ws_bytes, st, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pddp launch");
   return MCS_OK;
@@ -284,10 +300,11 @@ mcs_status mcs_dense_attn(const mcs_params* p, const void* q, const void* k, con
     return MCS_ERR_INVALID_ARG;
   const int BH = p->B * p->H;
   CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, q, BH, p->N, p->D) || !make_tile_map(&tk, k, BH, p->N, p->D) ||
-      !make_tile_map(&tv, v, BH, p->N, p->D))
+  if (!make_tile_map(&tq, q, p) || !make_tile_map(&tk, k, p) || !make_tile_map(&tv, v, p))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(tile)");
   mcs::AttnArgs a{};
+  a.H = p->H;
+  a.layout = p->layout;
   a.N = p->N;
   a.C = p->C;
   a.G = groups_of(p);

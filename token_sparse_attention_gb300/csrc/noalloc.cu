@@ -40,12 +40,9 @@ cudaError_t scratch_address(void** out) {
 
 extern "C" mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int32_t* perm,
                                         cudaStream_t stream) {
-  if (p == nullptr || q == nullptr || perm == nullptr) return MCS_ERR_INVALID_ARG;
-  if (p->B < 1 || p->H < 1 || p->N < 1 || (long long)p->B * p->H > 65535 ||
-      (long long)p->B * p->H * p->N > 0x7fffffffLL || p->pddp_iters < 0)
-    return MCS_ERR_INVALID_ARG;
-  if (p->D != 64 && p->D != 128) return MCS_ERR_UNSUPPORTED;
-  if (p->C != 64 && p->C != 128) return MCS_ERR_UNSUPPORTED;
+  const mcs_status st = mcs::check_params(p, false);
+  if (st != MCS_OK) return st;
+  if (q == nullptr || perm == nullptr) return MCS_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return MCS_ERR_INVALID_ARG;
   const int BH = p->B * p->H, N = p->N, D = p->D, C = p->C;
   const int G = (N + C - 1) / C;
@@ -64,15 +61,16 @@ extern "C" mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int3
   unsigned* status = nullptr;
   if ((e = mcs::device_status_word(&status)) != cudaSuccess) return MCS_ERR_CUDA;
 
+  // The kernels address q's rows by global head (either layout), so every
+  // batch uses the one gather map over all rows.
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
+  CUtensorMap tq;
+  if (!mcs::encode_gather_map(&tq, qb, static_cast<long long>(BH) * N, D)) return MCS_ERR_CUDA;
   for (int h0 = 0; h0 < BH; h0 += batch) {
     const int hc = BH - h0 < batch ? BH - h0 : batch;
-    const __nv_bfloat16* qh = qb + static_cast<size_t>(h0) * N * D;
-    CUtensorMap tq;
-    if (!mcs::encode_gather_map(&tq, qh, static_cast<long long>(hc) * N, D))
-      return MCS_ERR_CUDA;
-    e = mcs::launch_pddp(qh, &tq, hc, N, D, C, iters, perm + static_cast<size_t>(h0) * G * C,
-                         scratch, kNoallocScratchBytes, status, stream);
+    e = mcs::launch_pddp(qb, &tq, p->layout, p->H, h0, hc, N, D, C, iters,
+                         perm + static_cast<size_t>(h0) * G * C, scratch, kNoallocScratchBytes,
+                         status, stream);
     if (e != cudaSuccess) return MCS_ERR_CUDA;
   }
   return MCS_OK;

@@ -150,7 +150,7 @@ template <int D>
 __global__ void __launch_bounds__(kMomThreads, 2)
     pddp_moments_kernel(const __grid_constant__ CUtensorMap tq, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, int max_chunks, float* partials,
-                        unsigned* status) {
+                        unsigned* status, int layout, int H, int head0) {
   using L = MomLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kMomThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int32_t* pos = perm + (size_t)bh * N + nd.start + chunk * kChunkRows;
+  const RowMap rm = row_map(layout, H, N, head0 + bh);  // rows of q in either layout
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kMomThreads, 2)
         const int rr = j * 128 + 4 * lane + i;
         int t = rr < rows ? __ldg(pos + rr) : 0;
         if (t < 0 || t >= N) { bad = true; t = 0; }
-        r[i] = bh * N + t;
+        r[i] = rm.rbase + t * rm.rstride;
       }
       if (j >= 2) {
         bool ok = mbar_wait(empty + st, ((j >> 1) - 1) & 1, abort_flag, status);
@@ -397,7 +398,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
     pddp_project_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, const float* __restrict__ nodevec,
-                        uint64_t* __restrict__ keys) {
+                        uint64_t* __restrict__ keys, int layout, int H, int head0) {
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   const int bh = blockIdx.y;
   if (p >= N) return;
@@ -420,7 +421,8 @@ __global__ void __launch_bounds__(256)
   if ((nd.n + C - 1) / C <= 1) return;
   const int token = perm[(size_t)bh * N + p];
   const float* vec = nodevec + (size_t)(bh * slots + slot) * 2 * D;
-  const uint4* row = reinterpret_cast<const uint4*>(q + ((size_t)bh * N + token) * D);
+  const RowMap rm = row_map(layout, H, N, head0 + bh);
+  const uint4* row = reinterpret_cast<const uint4*>(q + (size_t)(rm.rbase + token * rm.rstride) * D);
   float t = 0.f;
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
@@ -576,8 +578,9 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int D>
-cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int BH, int N, int C, int iters,
-                     int32_t* perm_out, void* ws, unsigned* status, cudaStream_t stream) {
+cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int layout, int H, int head0,
+                     int BH, int N, int C, int iters, int32_t* perm_out, void* ws,
+                     unsigned* status, cudaStream_t stream) {
   const WsLayout w = ws_layout(BH, N, D, C);
   uint8_t* base = static_cast<uint8_t*>(ws);
   int32_t* pa = reinterpret_cast<int32_t*>(base + w.perm_a);
@@ -605,13 +608,13 @@ cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int BH, int 
     const int slots = 1 << d;
     const int chunks = (max_node_rows(N, C, d) + kChunkRows - 1) / kChunkRows;
     pddp_moments_kernel<D><<<dim3(chunks, slots, BH), kMomThreads, msmem, stream>>>(
-        *tq, pa, N, C, d, slots, chunks, partials, status);
+        *tq, pa, N, C, d, slots, chunks, partials, status, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     pddp_power_kernel<D><<<dim3(slots, BH), kPowThreads, psmem, stream>>>(partials, N, C, d, slots,
                                                                           chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    pddp_project_kernel<D><<<dim3((N + 255) / 256, BH), 256, 0, stream>>>(q, pa, N, C, d, slots,
-                                                                          nodevec, keys);
+    pddp_project_kernel<D><<<dim3((N + 255) / 256, BH), 256, 0, stream>>>(
+        q, pa, N, C, d, slots, nodevec, keys, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
                                                                      status);
@@ -628,12 +631,16 @@ cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int BH, int 
 
 size_t pddp_workspace_bytes(int BH, int N, int D, int C) { return ws_layout(BH, N, D, C).total; }
 
-cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int BH, int N, int D,
-                        int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,
-                        unsigned* status, cudaStream_t stream) {
+cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int layout, int H,
+                        int head0, int BH, int N, int D, int C, int iters, int32_t* perm_out,
+                        void* ws, size_t ws_bytes, unsigned* status, cudaStream_t stream) {
   if (ws_bytes < pddp_workspace_bytes(BH, N, D, C)) return cudaErrorInvalidValue;
-  if (D == 128) return run_pddp<128>(q, tq_gather, BH, N, C, iters, perm_out, ws, status, stream);
-  if (D == 64) return run_pddp<64>(q, tq_gather, BH, N, C, iters, perm_out, ws, status, stream);
+  if (D == 128)
+    return run_pddp<128>(q, tq_gather, layout, H, head0, BH, N, C, iters, perm_out, ws, status,
+                         stream);
+  if (D == 64)
+    return run_pddp<64>(q, tq_gather, layout, H, head0, BH, N, C, iters, perm_out, ws, status,
+                        stream);
   return cudaErrorInvalidValue;
 }
 

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     const int32_t* perm_g = a.perm + (static_cast<size_t>(bh) * a.G + g) * a.C;
-    const int rowbase = bh * a.N;
+    const RowMap rm = row_map(a.layout, a.H, a.N, bh);  // rows of q in either layout
     bool bad = false;
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
         int t = (p < a.C) ? __ldg(perm_g + p) : 0;
         if (t < 0) t = 0;
         if (t >= a.N) { bad = true; t = 0; }
-        r[i] = rowbase + t;
+        r[i] = rm.rbase + t * rm.rstride;
       }
       for (int s = 0; s < L::kSub; ++s)
         tma_gather4(sq + s * L::kQSub + r4 * 4 * 128, &tq, s * 64, r[0], r[1], r[2], r[3], q_full);
@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kMassThreads, 2)
       if (elect_one()) {
         mbar_expect_tx(k_full + st, L::kKStage);
         for (int s = 0; s < L::kSub; ++s)
-          tma_load_3d(sk + st * L::kKStage + s * L::kKSub, &tk, s * 64, j * 128, bh, k_full + st);
+          tma_load_4d(sk + st * L::kKStage + s * L::kKSub, &tk, s * 64, j * 128, bh % a.H,
+                      bh / a.H, k_full + st);
       }
       ++issued;
     }

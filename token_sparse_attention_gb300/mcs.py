@@ -49,19 +49,23 @@ class McsError(RuntimeError):
 
 
 class Params(ctypes.Structure):
-    """mcs_params: B, H, N, D, C, K, scale (0 -> 1/sqrt(D)), pddp_iters (0 -> 32)."""
+    """mcs_params: B, H, N, D, C, K, scale (0 -> 1/sqrt(D)), pddp_iters (0 -> 32),
+    layout (0: activations [B, H, N, D]; 1: [B, N, H, D])."""
 
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
                 ("D", ctypes.c_int), ("C", ctypes.c_int), ("K", ctypes.c_int),
-                ("scale", ctypes.c_float), ("pddp_iters", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("pddp_iters", ctypes.c_int), ("layout", ctypes.c_int)]
 
     @property
     def G(self) -> int:
         return -(-self.N // self.C)
 
 
-def params(B, H, N, D, C=128, K=None, scale=0.0, pddp_iters=0) -> Params:
-    return Params(B, H, N, D, C, N if K is None else K, scale, pddp_iters)
+LAYOUT_BHND, LAYOUT_BNHD = 0, 1
+
+
+def params(B, H, N, D, C=128, K=None, scale=0.0, pddp_iters=0, layout=LAYOUT_BHND) -> Params:
+    return Params(B, H, N, D, C, N if K is None else K, scale, pddp_iters, layout)
 
 
 def library_path() -> str:
@@ -149,7 +153,7 @@ def _check(status: int, where: str):
 
 
 def _qkv_shape(p: Params):
-    return (p.B, p.H, p.N, p.D)
+    return (p.B, p.N, p.H, p.D) if p.layout == LAYOUT_BNHD else (p.B, p.H, p.N, p.D)
 
 
 # ---------------------------------------------------------------- entry points
@@ -196,14 +200,14 @@ def mcs_dense_attn(p: Params, q, k, v, out, lse=None, stream=None):
     bf, s = torch.bfloat16, _qkv_shape(p)
     _check(lib().mcs_dense_attn(ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
                                 _ptr(v, bf, s, "v"), _ptr(out, bf, s, "out"),
-                                _ptr(lse, torch.float32, s[:3], "lse", optional=True),
+                                _ptr(lse, torch.float32, (p.B, p.H, p.N), "lse", optional=True),
                                 _stream(stream)), "mcs_dense_attn")
 
 
 def mcs_group_mass(p: Params, q, k, lse, perm, head_begin, head_count, mass, stream=None):
     bf, s = torch.bfloat16, _qkv_shape(p)
     _check(lib().mcs_group_mass(ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
-                                _ptr(lse, torch.float32, s[:3], "lse"),
+                                _ptr(lse, torch.float32, (p.B, p.H, p.N), "lse"),
                                 _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
                                 int(head_begin), int(head_count),
                                 _ptr(mass, torch.float32, (head_count, p.G, p.N), "mass"),
@@ -244,7 +248,7 @@ def mcs_select(p: Params, q, k, lse, perm, idx, ws, retained=None, stream=None):
     bf, s = torch.bfloat16, _qkv_shape(p)
     _check(lib().mcs_select(
         ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"),
-        _ptr(lse, torch.float32, s[:3], "lse"),
+        _ptr(lse, torch.float32, (p.B, p.H, p.N), "lse"),
         _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
         _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
         _ptr(retained, torch.float32, (p.B, p.H, p.G), "retained", optional=True),
@@ -258,7 +262,7 @@ def mcs_anchor_select(p: Params, q, k, v, perm, idx, dense_out, lse, residual, w
         ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"), _ptr(v, bf, s, "v"),
         _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
         _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
-        _ptr(dense_out, bf, s, "dense_out"), _ptr(lse, torch.float32, s[:3], "lse"),
+        _ptr(dense_out, bf, s, "dense_out"), _ptr(lse, torch.float32, (p.B, p.H, p.N), "lse"),
         _ptr(residual, bf, s, "residual"),
         _ptr(retained, torch.float32, (p.B, p.H, p.G), "retained", optional=True),
         _ptr(ws, torch.uint8, None, "ws"), ws.numel(), _stream(stream)), "mcs_anchor_select")
@@ -287,7 +291,7 @@ def meta_views(p: Params, entry: torch.Tensor):
     n_res = p.B * p.H * p.N * p.D * 2
     perm = entry[po:po + n_perm].view(torch.int32).view(p.B, p.H, p.G * p.C)
     idx = entry[io:io + n_idx].view(torch.int32).view(p.B, p.H, p.G, p.K)
-    res = entry[ro:ro + n_res].view(torch.bfloat16).view(p.B, p.H, p.N, p.D)
+    res = entry[ro:ro + n_res].view(torch.bfloat16).view(*_qkv_shape(p))
     return perm, idx, res
 
 
