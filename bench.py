@@ -302,27 +302,33 @@ def run_gpu(args, w, K, rank, world, dist):
     staging = None
     if not args.no_e2e:
         # The reuse step's inputs: Q, K, V from pinned host memory, and the
-        # layer's cached metadata (perm, idx, residual) as one entry staged by
-        # mcs_stager from pinned host memory into two device slots, each
-        # step's entry prefetched two steps ahead (one step ahead of the step
-        # that runs while it copies).
+        # layer's cached metadata (perm, idx as bitmaps, residual) as one
+        # entry staged by mcs_stager from pinned host memory into two device
+        # slots, each step's entry prefetched two steps ahead (one step ahead
+        # of the step that runs while it copies) and its index lists unpacked
+        # on the device before the step's sparse attention.
         hq, hk, hv = (t.cpu().pin_memory() for t in (q1, k1, v1))
         meta_bytes = mcs.mcs_meta_bytes(p)
-        hentry = torch.empty(meta_bytes, dtype=torch.uint8, pin_memory=True)
-        for dst, src in zip(mcs.meta_views(p, hentry), (perm, idx, res)):
-            dst.copy_(src.cpu())
         slots = [torch.empty(meta_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
         views = [mcs.meta_views(p, sl) for sl in slots]
+        views[0][0].copy_(perm)
+        views[0][2].copy_(res)
+        mcs.mcs_meta_pack(p, idx, slots[0])
+        hentry = torch.empty(meta_bytes, dtype=torch.uint8, pin_memory=True)
+        hentry.copy_(slots[0])
+        didx = torch.empty_like(idx)
         hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         sets = [[torch.empty_like(t) for t in (q1, k1, v1)] for _ in range(2)]
-        dout = torch.empty_like(out)
+        douts = [torch.empty_like(out) for _ in range(2)]
         host_in = (hq, hk, hv)
         h2d = sum(t.numel() * t.element_size() for t in host_in) + meta_bytes
         d2h = hout.numel() * hout.element_size()
-        copy_stream, meta_stream = torch.cuda.Stream(), torch.cuda.Stream()
+        copy_stream, meta_stream, d2h_stream = (torch.cuda.Stream() for _ in range(3))
         stager = mcs.Stager(p, slots, meta_stream)
         loaded = [torch.cuda.Event() for _ in range(2)]
         consumed = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read_back = [torch.cuda.Event() for _ in range(2)]
 
         def staged_run(n, with_qkv):
             for i in range(min(2, n)):
@@ -341,13 +347,22 @@ def run_gpu(args, w, K, rank, world, dist):
                 else:
                     dq, dk, dv = q1, k1, v1
                 stager.wait(s, stream)
-                dperm, didx, dres = views[s]
-                mcs.mcs_sparse_attn(p, dq, dk, dv, dperm, didx, dres, dout, stream=stream)
+                dperm, _, dres = views[s]
+                mcs.mcs_meta_unpack(p, slots[s], didx, stream=stream)
+                if with_qkv and i >= 2:
+                    stream.wait_event(read_back[s])  # output buffer s read back
+                mcs.mcs_sparse_attn(p, dq, dk, dv, dperm, didx, dres, douts[s], stream=stream)
                 consumed[s].record(stream)
                 if i + 2 < n:
                     stager.prefetch(s, hentry, after=stream)  # after this step read slot s
                 if with_qkv:
-                    hout.copy_(dout, non_blocking=True)
+                    # the result goes back to the host on its own stream, over
+                    # the link's other direction, while the next step runs
+                    computed[s].record(stream)
+                    with torch.cuda.stream(d2h_stream):
+                        d2h_stream.wait_event(computed[s])
+                        hout.copy_(douts[s], non_blocking=True)
+                        read_back[s].record(d2h_stream)
 
         def timed(with_qkv):
             staged_run(max(2, args.warmup), with_qkv)
@@ -358,7 +373,9 @@ def run_gpu(args, w, K, rank, world, dist):
             a.record(stream)
             copy_stream.wait_stream(stream)  # the first copies start after `a`
             meta_stream.wait_stream(stream)
+            d2h_stream.wait_stream(stream)
             staged_run(args.steps, with_qkv)
+            stream.wait_stream(d2h_stream)
             b.record(stream)  # after the last read-back, which follows every copy
             torch.cuda.synchronize()
             return a.elapsed_time(b) / args.steps
@@ -448,9 +465,11 @@ def run_gpu(args, w, K, rank, world, dist):
         "e2e": ({"value": job_tflops(world, flops_sparse, e2e_ms), "unit": "TFLOP/s",
                  "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                  "ms_per_step": e2e_ms,
-                 "pipelining": "step i+1's host->device copies overlap step i's kernel; "
-                               "the metadata entry (perm, idx, residual) is staged by "
-                               "mcs_stager into two device slots"}
+                 "pipelining": "step i+1's host->device copies and step i-1's "
+                               "device->host read-back overlap step i's kernel; "
+                               "the metadata entry (perm, idx bitmaps, residual) is staged "
+                               "by mcs_stager into two device slots and its indices "
+                               "unpacked on the device each step"}
                 if e2e else None),
         # Q, K, V resident; only the layer's metadata entry comes from pinned host
         # memory each step, prefetched ahead through mcs_stager (the cache offload

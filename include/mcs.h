@@ -232,14 +232,32 @@ mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int32_t* perm,
  * offloading inactive cache entries to CPU memory).
  *
  * An entry is one flat buffer of mcs_meta_bytes(p) bytes holding perm
- * [B,H,G*C] int32, idx [B,H,G,K] int32 and residual [B,H,N,D] bf16, each at
- * a 256-byte aligned offset (mcs_meta_offsets); host and device copies share
+ * [B,H,G*C] int32, the selected KV indices as bitmaps [B,H,G,ceil(N/32)]
+ * uint32 (bit j of group g's row set: token j kept; N/8 bytes per group
+ * instead of 4K) and residual (same shape and layout as q), each at a
+ * 256-byte aligned offset (mcs_meta_offsets); host and device copies share
  * the layout, so one copy moves an entry.  Both return 0 / MCS_ERR_* for
  * invalid params (K must be in [1, N]).
  */
 size_t mcs_meta_bytes(const mcs_params* p);
 mcs_status mcs_meta_offsets(const mcs_params* p, size_t* perm_off, size_t* idx_off,
                             size_t* residual_off);
+
+/*
+ * idx [B,H,G,K] (each row K distinct tokens in [0, N)) -> the bitmaps of the
+ * device entry (256-byte aligned).  A row with an index out of range or a
+ * repeated index sets MCS_ERR_BOUNDS in the device status.  N <= 1.6 M.
+ */
+mcs_status mcs_meta_pack(const mcs_params* p, const int32_t* idx, void* entry,
+                         cudaStream_t stream);
+
+/*
+ * The bitmaps of a device entry -> idx [B,H,G,K], each row ascending.  A row
+ * whose bitmap does not hold exactly K set bits sets MCS_ERR_BOUNDS in the
+ * device status (it writes at most K indices).  K <= 51200.
+ */
+mcs_status mcs_meta_unpack(const mcs_params* p, const void* entry, int32_t* idx,
+                           cudaStream_t stream);
 
 typedef struct mcs_stager mcs_stager;
 

@@ -94,7 +94,8 @@ def test_meta_entry_layout(L):
     G = p.G
     po, io, ro = mcs.mcs_meta_offsets(p)
     total = mcs.mcs_meta_bytes(p)
-    perm_b, idx_b, res_b = 40 * G * 128 * 4, 40 * G * 15120 * 4, 40 * 75600 * 128 * 2
+    # the indices are stored as bitmaps of N bits per group
+    perm_b, idx_b, res_b = 40 * G * 128 * 4, 40 * G * (-(-75600 // 32)) * 4, 40 * 75600 * 128 * 2
     assert po == 0 and io % 256 == 0 and ro % 256 == 0 and total % 256 == 0
     assert perm_b <= io < perm_b + 256
     assert idx_b <= ro - io < idx_b + 256
@@ -103,6 +104,15 @@ def test_meta_entry_layout(L):
     bad = mcs.params(1, 1, 100, 128, 64, 0)
     assert L.mcs_meta_bytes(ctypes.byref(bad)) == 0
     assert L.mcs_meta_offsets(ctypes.byref(bad), None, None, None) == 1
+
+
+def test_meta_pack_rejects_bad_arguments(L):
+    p = mcs.params(1, 2, 256, 128, 64, 40)
+    assert L.mcs_meta_pack(ctypes.byref(p), None, 256, None) == 1
+    assert L.mcs_meta_pack(ctypes.byref(p), 256, 256 + 16, None) == 1   # entry not 256-aligned
+    assert L.mcs_meta_unpack(ctypes.byref(p), 256, None, None) == 1
+    bad = mcs.params(1, 2, 256, 128, 64, 0)
+    assert L.mcs_meta_unpack(ctypes.byref(bad), 256, 256, None) == 1
 
 
 def test_stager_rejects_bad_arguments(L):

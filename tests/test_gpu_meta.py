@@ -1,7 +1,8 @@
-"""GPU tests of the metadata cache staging (mcs_meta_*, mcs_stager_*): entries
-offloaded to pinned host memory and prefetched back into device slots, one
-layer ahead, give the same reuse-step outputs as metadata kept on the device.
-Every call goes through the C ABI (libmcs.so)."""
+"""GPU tests of the metadata cache staging (mcs_meta_*, mcs_stager_*): index
+lists packed into bitmaps and unpacked again are unchanged; entries offloaded
+to pinned host memory and prefetched back into device slots, one layer ahead,
+give the same reuse-step outputs as metadata kept on the device.  Every call
+goes through the C ABI (libmcs.so)."""
 
 import numpy as np
 import pytest
@@ -24,12 +25,16 @@ def _lib():
 
 
 def _anchor_into(p, q, k, v, entry):
-    """Anchor step whose perm / idx / residual land in a device entry."""
-    perm, idx, res = mcs.meta_views(p, entry)
+    """Anchor step whose perm and residual land in a device entry and whose
+    indices are packed into it; returns the index list."""
+    perm, _, res = mcs.meta_views(p, entry)
+    idx = torch.empty(p.B, p.H, p.G, p.K, dtype=torch.int32, device="cuda")
     dense = torch.empty_like(q)
     lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device="cuda")
     ws = mcs.empty_workspace(mcs.mcs_anchor_workspace(p))
     mcs.mcs_anchor_select(p, q, k, v, perm, idx, dense, lse, res, ws)
+    mcs.mcs_meta_pack(p, idx, entry)
+    return idx
 
 
 def _layer_inputs(w, layer):
@@ -40,13 +45,44 @@ def _layer_inputs(w, layer):
     return (q0, k0, v0), (q1, k1, v1)
 
 
+@pytest.mark.parametrize("N,K,C", [(5000, 1000, 128), (4099, 4099, 64), (300, 1, 64),
+                                   (70, 33, 64)])
+def test_pack_unpack_round_trip(N, K, C):
+    B, H = 2, 2
+    p = mcs.params(B, H, N, 64, C, K)
+    rng = np.random.default_rng(N + K)
+    idx = np.stack([np.sort(rng.choice(N, K, replace=False)) for _ in range(B * H * p.G)])
+    idx = torch.from_numpy(idx.astype(np.int32)).view(B, H, p.G, K).cuda()
+    entry = torch.full((mcs.mcs_meta_bytes(p),), 0x5A, dtype=torch.uint8, device="cuda")
+    mcs.mcs_meta_pack(p, idx, entry)
+    got = torch.full_like(idx, -7)
+    mcs.mcs_meta_unpack(p, entry, got)
+    assert mcs.mcs_device_status() == 0
+    assert torch.equal(got, idx)
+    # the bitmap itself: bit j of a group's row set exactly for its indices
+    _, bits, _ = mcs.meta_views(p, entry)
+    b = bits[0, 0, 0].cpu().numpy().view(np.uint32)
+    want = np.zeros(b.size, dtype=np.uint32)
+    for j in idx[0, 0, 0].cpu().numpy():
+        want[j >> 5] |= np.uint32(1) << np.uint32(j & 31)
+    np.testing.assert_array_equal(b, want)
+
+
+def test_pack_reports_repeated_index():
+    p = mcs.params(1, 1, 256, 64, 64, 4)
+    idx = torch.tensor([[3, 3, 5, 9]] * p.G, dtype=torch.int32).view(1, 1, p.G, 4).cuda()
+    entry = torch.empty(mcs.mcs_meta_bytes(p), dtype=torch.uint8, device="cuda")
+    mcs.mcs_meta_pack(p, idx, entry)
+    assert mcs.mcs_device_status() == 6   # MCS_ERR_BOUNDS, and the word is cleared
+
+
 def test_offload_prefetch_round_trip():
     w = synth.workload("tiny")
     p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
     nbytes = mcs.mcs_meta_bytes(p)
     dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     (q0, k0, v0), _ = _layer_inputs(w, 0)
-    _anchor_into(p, q0, k0, v0, dev)
+    idx = _anchor_into(p, q0, k0, v0, dev)
     want = dev.clone()
     host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     copy = torch.cuda.Stream()
@@ -58,10 +94,11 @@ def test_offload_prefetch_round_trip():
     st.prefetch(0, host, after=cur)
     st.wait(0, cur)
     got = dev.clone()         # ordered after the prefetch by the wait
+    back = torch.empty_like(idx)
+    mcs.mcs_meta_unpack(p, dev, back)
     torch.cuda.synchronize()
     assert torch.equal(got, want)
-    perm, idx, res = mcs.meta_views(p, host)
-    assert torch.equal(idx, mcs.meta_views(p, want.cpu())[1])
+    assert torch.equal(back, idx)
     st.close()
 
 
@@ -72,11 +109,11 @@ def test_layer_pipeline_prefetch_one_ahead_matches_resident():
     p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2))
     L = 3
     nbytes = mcs.mcs_meta_bytes(p)
-    resident, hosts, reuse_in = [], [], []
+    resident, hosts, reuse_in, idxs = [], [], [], []
     for layer in range(L):
         (q0, k0, v0), (q1, k1, v1) = _layer_inputs(w, 2 * layer)
         e = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        _anchor_into(p, q0, k0, v0, e)
+        idxs.append(_anchor_into(p, q0, k0, v0, e))
         resident.append(e)
         reuse_in.append((q1, k1, v1))
     copy = torch.cuda.Stream()
@@ -92,31 +129,34 @@ def test_layer_pipeline_prefetch_one_ahead_matches_resident():
         hosts.append(h)
     torch.cuda.synchronize()
     off.close()
-    # resident reference outputs
+    # resident reference outputs, from the anchor's own index lists
     want = []
     for layer in range(L):
-        perm, idx, res = mcs.meta_views(p, resident[layer])
+        perm, _, res = mcs.meta_views(p, resident[layer])
         q1, k1, v1 = reuse_in[layer]
         out = torch.empty_like(q1)
-        mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idx, res, out)
+        mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idxs[layer], res, out)
         want.append(out)
-    # staged: two slots, prefetch one layer ahead
+    # staged: two slots, prefetch one layer ahead, indices unpacked per layer
     slots = [torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda") for _ in range(2)]
     st = mcs.Stager(p, slots, copy)
     st.prefetch(0, hosts[0], after=cur)
+    idx = torch.empty(p.B, p.H, p.G, p.K, dtype=torch.int32, device="cuda")
     got = []
     for layer in range(L):
         s = layer % 2
         if layer + 1 < L:
             st.prefetch(1 - s, hosts[layer + 1], after=cur)
         st.wait(s, cur)
-        perm, idx, res = mcs.meta_views(p, slots[s])
+        perm, _, res = mcs.meta_views(p, slots[s])
+        mcs.mcs_meta_unpack(p, slots[s], idx)
         q1, k1, v1 = reuse_in[layer]
         out = torch.empty_like(q1)
         mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idx, res, out)
         got.append(out)
     torch.cuda.synchronize()
     st.close()
+    assert mcs.mcs_device_status() == 0
     for layer in range(L):
         np.testing.assert_array_equal(got[layer].view(torch.int16).cpu().numpy(),
                                       want[layer].view(torch.int16).cpu().numpy())

@@ -22,7 +22,7 @@ __all__ = [
     "mcs_group_workspace", "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn",
     "mcs_group_mass", "mcs_topk", "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record",
     "mcs_anchor_select", "mcs_group_noalloc", "mcs_meta_bytes", "mcs_meta_offsets",
-    "meta_views", "Stager", "mcs_block_workspace", "mcs_block_topk", "mcs_pooled_block_select",
+    "meta_views", "mcs_meta_pack", "mcs_meta_unpack", "Stager", "mcs_block_workspace", "mcs_block_topk", "mcs_pooled_block_select",
     "mcs_gather_mass", "mcs_rel_l1",
 ]
 
@@ -31,7 +31,8 @@ EXPORTED = (
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
     "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
-    "mcs_meta_bytes", "mcs_meta_offsets", "mcs_stager_create", "mcs_stager_destroy",
+    "mcs_meta_bytes", "mcs_meta_offsets", "mcs_meta_pack", "mcs_meta_unpack",
+    "mcs_stager_create", "mcs_stager_destroy",
     "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait", "mcs_block_workspace",
     "mcs_block_topk", "mcs_pooled_block_select", "mcs_gather_mass", "mcs_rel_l1",
 )
@@ -93,6 +94,8 @@ _SIGS = {
     "mcs_group_noalloc": ([_pp, _vp, _vp, _vp], _st),
     "mcs_meta_bytes": ([_pp], _sz),
     "mcs_meta_offsets": ([_pp, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)], _st),
+    "mcs_meta_pack": ([_pp, _vp, _vp, _vp], _st),
+    "mcs_meta_unpack": ([_pp, _vp, _vp, _vp], _st),
     "mcs_stager_create": ([_pp, _i, ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp)], _st),
     "mcs_stager_destroy": ([_vp], None),
     "mcs_stager_prefetch": ([_vp, _i, _vp, _vp], _st),
@@ -280,19 +283,34 @@ def mcs_meta_offsets(p: Params) -> tuple[int, int, int]:
 
 
 def meta_views(p: Params, entry: torch.Tensor):
-    """(perm, idx, residual) views into a metadata entry (uint8, host or device)."""
+    """(perm, bits, residual) views into a metadata entry (uint8, host or
+    device); bits [B, H, G, ceil(N/32)] holds the index bitmaps (as int32)."""
     if entry.dtype != torch.uint8 or not entry.is_contiguous() or entry.dim() != 1:
         raise ValueError("entry must be a contiguous 1-D uint8 tensor")
     if entry.numel() < mcs_meta_bytes(p):
         raise ValueError("entry is smaller than mcs_meta_bytes(p)")
     po, io, ro = mcs_meta_offsets(p)
     n_perm = p.B * p.H * p.G * p.C * 4
-    n_idx = p.B * p.H * p.G * p.K * 4
+    W = -(-p.N // 32)
+    n_idx = p.B * p.H * p.G * W * 4
     n_res = p.B * p.H * p.N * p.D * 2
     perm = entry[po:po + n_perm].view(torch.int32).view(p.B, p.H, p.G * p.C)
-    idx = entry[io:io + n_idx].view(torch.int32).view(p.B, p.H, p.G, p.K)
+    idx = entry[io:io + n_idx].view(torch.int32).view(p.B, p.H, p.G, W)
     res = entry[ro:ro + n_res].view(torch.bfloat16).view(*_qkv_shape(p))
     return perm, idx, res
+
+
+def mcs_meta_pack(p: Params, idx, entry, stream=None):
+    _check(lib().mcs_meta_pack(ctypes.byref(p),
+                               _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+                               _ptr(entry, torch.uint8, None, "entry"), _stream(stream)),
+           "mcs_meta_pack")
+
+
+def mcs_meta_unpack(p: Params, entry, idx, stream=None):
+    _check(lib().mcs_meta_unpack(ctypes.byref(p), _ptr(entry, torch.uint8, None, "entry"),
+                                 _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+                                 _stream(stream)), "mcs_meta_unpack")
 
 
 class Stager:
