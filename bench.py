@@ -47,11 +47,13 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, with the
 # sha1 of the kernel source it was measured on (traffic is reported only
-# while the source is unchanged).  Filled from profiles/.
+# while the source is unchanged).
 TRAFFIC = {
-    # ncu dram bytes (read + write) of the sparse reuse launch of the 4-head
-    # large workload, times 10 for the 40-head launch (heads are independent)
-    "attn.cu": {"sha": "96176a4dc22a", "bytes_per_launch": 10 * (664201216 + 69140480)},
+    # ncu dram bytes (read + write) of the sparse reuse launch of the 40-head
+    # large workload, one-pass capture at full size (mean of the two timed
+    # launches of `bench.py --steps 2 --warmup 1 --no-e2e --no-cpu-baseline`)
+    "attn.cu": {"sha": "1e2afdf3b6cf",
+                "bytes_per_launch": (6478033920 + 763077376 + 6466837760 + 762905344) // 2},
 }
 
 
