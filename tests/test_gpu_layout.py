@@ -86,3 +86,35 @@ def test_bad_layout_is_rejected_before_launch():
     q = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mcs.McsError):
         mcs.mcs_dense_attn(p, q, q, q, torch.empty_like(q))
+
+
+def test_large_workload_dense_and_reuse_layout_independent():
+    # full size (40 heads of 75600 tokens), the launches the benchmark times
+    from token_sparse_attention_gb300 import synth
+    w = synth.workload("large")
+    K = w.K(0.2)
+    q, k, v = synth.make_qkv(w, 0, device="cuda")
+    p0 = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
+    p1 = mcs.params(w.B, w.H, w.N, w.D, w.C, K, layout=mcs.LAYOUT_BNHD)
+    G = p0.G
+    # groups and indices: any valid ones (a strided selection per group)
+    perm = torch.arange(G * w.C, dtype=torch.int32, device="cuda").clamp_max(w.N - 1)
+    perm[w.N:] = -1
+    perm = perm.expand(w.B, w.H, -1).contiguous()
+    step = w.N // K
+    idx = (torch.arange(K, dtype=torch.int32, device="cuda") * step)
+    idx = (idx[None, :] + torch.arange(G, dtype=torch.int32, device="cuda")[:, None] % step)
+    idx = idx.expand(w.B, w.H, G, K).contiguous()
+    res = (0.01 * q).contiguous()
+    outs = {}
+    for p, cv in ((p0, lambda t: t), (p1, bnhd)):
+        d = torch.empty_like(cv(q))
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+        mcs.mcs_dense_attn(p, cv(q), cv(k), cv(v), d, lse)
+        o = torch.empty_like(d)
+        mcs.mcs_sparse_attn(p, cv(q), cv(k), cv(v), perm, idx, cv(res), o)
+        assert mcs.mcs_device_status() == 0
+        outs[p.layout] = (cv(d), lse, cv(o))   # bnhd() is its own inverse
+        del d, o
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)

@@ -5,8 +5,10 @@ The oracle cannot run whole heads of 75600 queries, so each workload is
 checked on sampled units the oracle computes one by one, plus properties that
 hold at any size:
   * the whole anchor step on the GPU: valid groups for every head, selected
-    indices ascending and in range, retained mass at most the group size, and
-    reuse with the anchor's own inputs reproducing the dense output;
+    indices ascending and in range, retained mass at most the group size, the
+    fused selection equal to group mass + radix top-K on head 0, index sets
+    unchanged through the metadata entry's bitmaps, and reuse with the
+    anchor's own inputs reproducing the dense output;
   * dense attention and LSE on sampled query rows of two heads;
   * group mass, top-K and sparse attention (+ residual) on sampled groups of
     head 0, with the groups, LSE values and indices made by the oracle;
@@ -67,6 +69,22 @@ def test_workload_full_size(name, density):
     for h in (0, BH - 1):
         ih = idx.view(BH, G, K)[h].cpu().numpy()
         assert ih.min() >= 0 and ih.max() < w.N and np.all(np.diff(ih, axis=1) > 0)
+    # the anchor's fused selection (mass histogram + one-read top-K) against
+    # mcs_group_mass + mcs_topk (four-read radix select) on the same groups and
+    # LSE: identical index sets for head 0
+    m0 = torch.empty(1, G, w.N, dtype=torch.float32, device="cuda")
+    mcs.mcs_group_mass(p, q, k, lse, perm, 0, 1, m0)
+    s0 = torch.empty(G, K, dtype=torch.int32, device="cuda")
+    mcs.mcs_topk(p, m0, s0)
+    assert torch.equal(s0, idx.view(BH, G, K)[0]), f"{name}: fused selection differs"
+    del m0, s0
+    # the metadata entry's index bitmaps carry every head's sets unchanged
+    entry = torch.empty(mcs.mcs_meta_bytes(p), dtype=torch.uint8, device="cuda")
+    mcs.mcs_meta_pack(p, idx, entry)
+    back = torch.empty_like(idx)
+    mcs.mcs_meta_unpack(p, entry, back)
+    assert mcs.mcs_device_status() == 0 and torch.equal(back, idx)
+    del entry, back
     same = torch.empty_like(q)
     mcs.mcs_sparse_attn(p, q, k, v, perm, idx, res, same)
     d = (same.float() - dense.float()).abs()
