@@ -423,7 +423,7 @@ def run_gpu(args, w, K, rank, world, dist):
     # mcs_select passes the heads through the workspace in chunks; each chunk
     # is one group-mass and one top-K launch
     rup = lambda x: -(-x // 256) * 256  # noqa: E731
-    chunk = max(1, min(BH, ws_bytes // (rup(G * w.N * 4) + rup(G * 2048 * 4))))
+    chunk = max(1, min(BH, ws_bytes // (rup(G * w.N * 4) + rup(G * 1088 * 4))))
     n_chunks = -(-BH // chunk)
     launches = (2 + 4 * depths) + 1 + 2 * n_chunks + 1 + 1
     cores = len(os.sched_getaffinity(0))

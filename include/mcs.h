@@ -150,7 +150,7 @@ mcs_status mcs_topk(const mcs_params* p, const float* mass, int rows, int32_t* i
  * masse) is selected in four reads instead.
  * ws: device workspace through which the masses and histograms pass, heads
  * in chunks: mcs_anchor_workspace(p) bytes process every head at once (up to
- * 4 GiB); at least G*(N+2048)*4 bytes (each part rounded up to 256) are
+ * 4 GiB); at least G*(N+1088)*4 bytes (each part rounded up to 256) are
  * needed.  Requires K <= N.
  */
 mcs_status mcs_select(const mcs_params* p, const void* q, const void* k, const float* lse,
@@ -187,7 +187,7 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
  * output) and lse; a3 + a4 exact selection (as mcs_select) -> idx (and
  * retained mass [B,H,G], nullable); a5 anchor form -> residual.
  * ws: device workspace of at least mcs_anchor_workspace(p) bytes; a smaller
- * one (but at least one head's group masses and histograms, G*(N+2048)*4
+ * one (but at least one head's group masses and histograms, G*(N+1088)*4
  * bytes rounded up to 256-byte multiples, and the grouping workspace)
  * processes fewer heads per selection pass.
  */

@@ -75,6 +75,12 @@ cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUten
                              const CUtensorMap* tv, const AttnArgs& a, int BH,
                              cudaStream_t stream);
 
+// Bins of the group-mass digit histogram: digit = top 12 bits of the fp32
+// mass (sign, exponent, three mantissa bits).  A group's masses are at most
+// its size C <= 128 (up to rounding), whose digits are <= 1072; larger digits
+// (masses of 256 or more, infinities, NaNs) fall in the last bin.
+constexpr int kMassHistBins = 1088;
+
 struct MassArgs {
   int H, layout;          // heads per batch entry; tensor layout (see RowMap)
   int N, C, G;
@@ -83,7 +89,7 @@ struct MassArgs {
   const int32_t* perm;    // [BH, G*C]
   const float* lse;       // [BH, N]
   float* mass;            // [heads in chunk, G, N]
-  uint32_t* hist;         // [heads in chunk, G, 2048] digit counts of each mass row, or null
+  uint32_t* hist;         // [heads in chunk, G, kMassHistBins] digit counts per mass row, or null
   unsigned* status;
 };
 
@@ -92,7 +98,7 @@ cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* t
                               const MassArgs& a, int heads, cudaStream_t stream);
 
 // rows x n masses -> rows x K ascending indices (+ retained sums, nullable).
-// hist (nullable): each row's 2048-bin digit histogram written by the mass
+// hist (nullable): each row's digit histogram written by the mass
 // kernel; with it most rows are selected in one read of their masses.
 cudaError_t launch_topk(const float* mass, const uint32_t* hist, int rows, int n, int K,
                         int32_t* idx, float* retained, unsigned* status, cudaStream_t stream);

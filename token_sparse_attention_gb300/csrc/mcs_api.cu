@@ -163,10 +163,9 @@ size_t mass_head_bytes(const mcs_params* p) {
 }
 
 // Workspace per head of the anchor step's selection: the group masses and
-// their 2048-bin digit histograms.
-constexpr size_t kHistBins = 2048;
+// their digit histograms (kMassHistBins words per group).
 size_t hist_head_bytes(const mcs_params* p) {
-  return static_cast<size_t>(groups_of(p)) * kHistBins * sizeof(uint32_t);
+  return static_cast<size_t>(groups_of(p)) * mcs::kMassHistBins * sizeof(uint32_t);
 }
 size_t select_head_bytes(const mcs_params* p) {
   return round_up(mass_head_bytes(p), 256) + round_up(hist_head_bytes(p), 256);
@@ -366,7 +365,7 @@ mcs_status mcs_select(const mcs_params* p, const void* q, const void* k, const f
   const int BH = p->B * p->H;
   const int G = groups_of(p);
   // a chunk of heads at a time through the workspace: the masses [chunk, G, N],
-  // then their digit histograms [chunk, G, 2048]
+  // then their digit histograms [chunk, G, kMassHistBins]
   const int chunk = static_cast<int>(std::min<size_t>(BH, ws_bytes / per_head));
   float* mass = static_cast<float*>(ws);
   uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) +

@@ -277,6 +277,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// As sdesc_sw128 without swizzle (mode 0), for small K-major operands stored
+// as 8-row x 16-byte core matrices: LBO = byte distance between the core
+// matrices adjacent along K, SBO = between those adjacent along M/N.
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // Bits: D format (4-5) = 1 (f32); A format (7-9) = 1 (bf16); B format
 // (10-12) = 1 (bf16); A major (15), B major (16): 0 = K-major, 1 = MN-major;

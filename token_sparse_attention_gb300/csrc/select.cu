@@ -37,8 +37,8 @@ namespace {
 constexpr int kMassThreads = 192;
 // Histogram digit of a mass: the float's top 12 bits (sign, exponent, three
 // mantissa bits; masses are >= 0, so the digit grows with the mass), clamped
-// so that a NaN with the sign bit set stays in range.
-constexpr int kHistBins = 2048;
+// to the last bin (kMassHistBins in internal.h).
+constexpr int kHistBins = kMassHistBins;
 __device__ __forceinline__ uint32_t mass_digit(uint32_t bits) {
   return min(bits >> 20, static_cast<uint32_t>(kHistBins - 1));
 }
@@ -51,8 +51,12 @@ struct MassLayout {
   static constexpr int kQ = 0;
   static constexpr int kK0 = kSub * kQSub;      // 1024-aligned (CQ multiple of 8)
   static constexpr int kKStage = kSub * kKSub;
-  static constexpr int kBias = kK0 + 2 * kKStage;
-  static constexpr int kHist = kBias + CQ * 4;           // mass histogram (kHistBins words)
+  // the bias step's operands: a ones tile (128 KV rows x 16) and the
+  // queries' bias parts (CQ rows x 16), K-major without swizzle, 8-row x
+  // 16-byte core matrices, the two K halves of an 8-row group adjacent
+  static constexpr int kOnes = kK0 + 2 * kKStage;
+  static constexpr int kQb = kOnes + 128 * 32;
+  static constexpr int kHist = kQb + CQ * 32;            // mass histogram (kHistBins words)
   static constexpr int kBars = kHist + kHistBins * 4;
   static constexpr int kUsed = kBars + 128 + 1024;
   // at most two CTAs per SM (TMEM: 2 x 256 columns)
@@ -83,7 +87,8 @@ __global__ void __launch_bounds__(kMassThreads, 2)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sq = smem + L::kQ;
   uint8_t* sk = smem + L::kK0;
-  float* bias = reinterpret_cast<float*>(smem + L::kBias);
+  uint8_t* sones = smem + L::kOnes;
+  uint8_t* sqb = smem + L::kQb;
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem + L::kHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* q_full = bars + 0;
@@ -116,6 +121,44 @@ __global__ void __launch_bounds__(kMassThreads, 2)
   if (warp == 5) {
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
+  }
+  // The bias of query p enters the scores through the MMA: one more K step of
+  // 16 multiplies a ones tile (KV rows) by the query's -lse/scale, split into
+  // three bf16 parts whose sum is exact to ~2^-24 relative, so that the exp
+  // warps compute exp2(scale*log2(e) * S') with S' = q.k - lse/scale straight
+  // from TMEM.  Padding slots get a large negative bias (probability 0).
+  if (threadIdx.x < 128) {
+    const int r = threadIdx.x;
+    const int core = ((r >> 3) * 2) * 128 + (r & 7) * 16;  // K half 0; half 1 at +128
+    const __nv_bfloat16 one = __float2bfloat16_rn(1.f), zero = __float2bfloat16_rn(0.f);
+    __nv_bfloat162 v01 = __halves2bfloat162(one, one), v23 = __halves2bfloat162(one, zero);
+    uint4 w0;
+    w0.x = *reinterpret_cast<uint32_t*>(&v01);
+    w0.y = *reinterpret_cast<uint32_t*>(&v23);
+    w0.z = 0u;
+    w0.w = 0u;
+    *reinterpret_cast<uint4*>(sones + core) = w0;
+    *reinterpret_cast<uint4*>(sones + core + 128) = make_uint4(0u, 0u, 0u, 0u);
+    if (r < CQ) {
+      constexpr float kLog2e = 1.4426950408889634f;
+      const int p = (r < a.C) ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g) * a.C + r) : -1;
+      float b = -1e30f;
+      if (p >= 0 && p < a.N)
+        b = -(__ldg(a.lse + static_cast<size_t>(bh) * a.N + p) * kLog2e) / a.scale_log2;
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(b);
+      const float r1 = b - __bfloat162float(h0);
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 h2 = __float2bfloat16_rn(r1 - __bfloat162float(h1));
+      __nv_bfloat162 p01 = __halves2bfloat162(h0, h1), p23 = __halves2bfloat162(h2, zero);
+      uint4 wb;
+      wb.x = *reinterpret_cast<uint32_t*>(&p01);
+      wb.y = *reinterpret_cast<uint32_t*>(&p23);
+      wb.z = 0u;
+      wb.w = 0u;
+      *reinterpret_cast<uint4*>(sqb + core) = wb;
+      *reinterpret_cast<uint4*>(sqb + core + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
   }
   tc_fence_before();
   __syncthreads();
@@ -170,6 +213,8 @@ __global__ void __launch_bounds__(kMassThreads, 2)
     // whole warp in the loop, one elected lane issues each tile's MMAs
     constexpr uint32_t idesc = idesc_bf16(128, CQ, false, false);
     const uint32_t q_addr = smem_u32(sq), k_addr = smem_u32(sk);
+    const uint64_t ones_desc = sdesc_none(smem_u32(sones), 128, 256);
+    const uint64_t qb_desc = sdesc_none(smem_u32(sqb), 128, 256);
     bool ok = warp_wait_m(q_full, 0, abort_flag, a.status);
     for (int j = 0; ok && j < ntiles; ++j) {
       const int st = j & 1;
@@ -185,6 +230,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
           umma_ss(tmem + st * CQ, sdesc_sw128(kb + ko, 16, 1024), sdesc_sw128(q_addr + qo, 16, 1024),
                   idesc, kk > 0);
         }
+        umma_ss(tmem + st * CQ, ones_desc, qb_desc, idesc, 1u);  // + bias of each query
         umma_commit(s_full + st);
         umma_commit(k_empty + st);
       }
@@ -196,18 +242,11 @@ __global__ void __launch_bounds__(kMassThreads, 2)
     // ------------------------------------------------------------ exp + sum
     const int t = threadIdx.x;  // 0..127: KV row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    constexpr float kLog2e = 1.4426950408889634f;
-    if (t < CQ) {
-      const int p = (t < a.C) ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g) * a.C + t) : -1;
-      bias[t] = (p >= 0 && p < a.N) ? __ldg(a.lse + static_cast<size_t>(bh) * a.N + p) * kLog2e
-                                    : INFINITY;
-    }
     if (a.hist != nullptr)
       for (int b = t; b < kHistBins; b += 128) shist[b] = 0;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const float sl2 = a.scale_log2;
     float* mass_row = a.mass + (static_cast<size_t>(hc) * a.G + g) * a.N;
-    const float4* bias4 = reinterpret_cast<const float4*>(bias);
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       if (!warp_wait_m(s_full + st, (j >> 1) & 1, abort_flag, a.status)) break;
@@ -219,13 +258,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
         tmem_ld32(tmem + st * CQ + lane_off + c * 32, s);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 b = bias4[(c * 32 + i) >> 2];
-          acc += ex2(fmaf(__uint_as_float(s[i + 0]), sl2, -b.x));
-          acc += ex2(fmaf(__uint_as_float(s[i + 1]), sl2, -b.y));
-          acc += ex2(fmaf(__uint_as_float(s[i + 2]), sl2, -b.z));
-          acc += ex2(fmaf(__uint_as_float(s[i + 3]), sl2, -b.w));
-        }
+        for (int i = 0; i < 32; ++i) acc += ex2(__uint_as_float(s[i]) * sl2);
       }
       tc_fence_before();
       __syncwarp();
@@ -453,8 +486,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 
   // 1. threshold digit (two bins per thread, counted from the top)
   const uint32_t* hrow = hist + row * kHistBins;
-  const int first = kHistBins - 1 - 2 * tid;
-  const uint32_t c0 = hrow[first], c1 = hrow[first - 1];
+  static_assert(2 * kTopkThreads >= kHistBins, "two bins per thread cover the histogram");
+  const int first = kHistBins - 1 - 2 * tid;  // < 0 for the threads past the last bin
+  const uint32_t c0 = first >= 0 ? hrow[first] : 0u, c1 = first >= 1 ? hrow[first - 1] : 0u;
   if (tid == 0) {
     scal[0] = kHistBins;  // not found
     scal[1] = 0;
