@@ -334,13 +334,31 @@ __global__ void __launch_bounds__(kPowThreads)
   const int tid = threadIdx.x;
   constexpr int LD = D + 1;
   const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * (D * D + D);
-  for (int i = tid; i < D * D + D; i += kPowThreads) {
-    float acc = 0.f;
-    for (int c = 0; c < nchunks; ++c) acc += base[(size_t)c * (D * D + D) + i];
-    if (i < D * D)
-      cov[(i / D) * LD + (i % D)] = acc;
-    else
-      s[i - D * D] = acc;
+  // Sum the chunks' partial moments: each thread takes 8 elements at once so
+  // that 8 independent loads per chunk are in flight (one element per thread
+  // made every load wait for the previous one).
+  constexpr int DD = D * D + D;
+  constexpr int kU = 8;
+  for (int i0 = tid; i0 < DD; i0 += kU * kPowThreads) {
+    float acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const float* pc = base + (size_t)c * DD;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kPowThreads;
+        if (i < DD) acc[u] += __ldg(pc + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kPowThreads;
+      if (i < D * D)
+        cov[(i / D) * LD + (i % D)] = acc[u];
+      else if (i < DD)
+        s[i - D * D] = acc[u];
+    }
   }
   __syncthreads();
   const float inv_n = 1.f / static_cast<float>(nd.n);
