@@ -239,7 +239,11 @@ def run_gpu(args, w, K, rank, world, dist):
         return t.transpose(1, 2).contiguous() if layout == mcs.LAYOUT_BNHD else t
 
     q0, k0, v0 = (lay(t) for t in synth.make_qkv(w, 0, device=dev))
-    q1, k1, v1 = (lay(t) for t in synth.make_qkv(w, 1, device=dev))
+    # the anchor's metadata serves the next R denoising steps, each with its
+    # own inputs (the generator's steps 1..R)
+    R = args.reuse_per_anchor
+    reuse_in = [tuple(lay(t) for t in synth.make_qkv(w, s_, device=dev)) for s_ in range(1, R + 1)]
+    q1, k1, v1 = reuse_in[0]
     perm = torch.empty(w.B, w.H, G * w.C, dtype=torch.int32, device=dev)
     idx = torch.empty(w.B, w.H, G, K, dtype=torch.int32, device=dev)
     dense = torch.empty_like(q0)
@@ -250,7 +254,7 @@ def run_gpu(args, w, K, rank, world, dist):
     ws_bytes = mcs.mcs_anchor_workspace(p)
     ws = mcs.empty_workspace(ws_bytes, dev)
     stream = torch.cuda.current_stream()
-    stages = ["pddp", "dense", "select", "record", "reuse"]
+    stages = ["pddp", "dense", "select", "record"] + [f"reuse{r}" for r in range(R)]
 
     def step(ev):
         ev[0].record(stream)
@@ -262,8 +266,9 @@ def run_gpu(args, w, K, rank, world, dist):
         ev[3].record(stream)
         mcs.mcs_sparse_attn_record(p, q0, k0, v0, perm, idx, dense, res)
         ev[4].record(stream)
-        mcs.mcs_sparse_attn(p, q1, k1, v1, perm, idx, res, out)
-        ev[5].record(stream)
+        for r, (qr, kr, vr) in enumerate(reuse_in):
+            mcs.mcs_sparse_attn(p, qr, kr, vr, perm, idx, res, out)
+            ev[5 + r].record(stream)
 
     def new_events():
         return [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
@@ -291,6 +296,8 @@ def run_gpu(args, w, K, rank, world, dist):
     total_ms = start.elapsed_time(end)
     stage_ms = {s: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs)
                 for k, s in enumerate(stages)}
+    reuse_launch_ms = [stage_ms.pop(f"reuse{r}") for r in range(R)]
+    stage_ms["reuse"] = statistics.mean(reuse_launch_ms)  # the metric's kernel
     st = mcs.mcs_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {mcs.mcs_status_string(st)}")
@@ -425,7 +432,7 @@ def run_gpu(args, w, K, rank, world, dist):
     rup = lambda x: -(-x // 256) * 256  # noqa: E731
     chunk = max(1, min(BH, ws_bytes // (rup(G * w.N * 4) + rup(G * 1088 * 4))))
     n_chunks = -(-BH // chunk)
-    launches = (2 + 4 * depths) + 1 + 2 * n_chunks + 1 + 1
+    launches = (2 + 4 * depths) + 1 + 2 * n_chunks + 1 + R
     cores = len(os.sched_getaffinity(0))
     cpu = None
     if not args.no_cpu_baseline:
@@ -448,8 +455,11 @@ def run_gpu(args, w, K, rank, world, dist):
         "config": {
             "workload": f"{w.name} B={w.B} H={w.H} N={w.N} D={w.D} C={w.C} "
                         f"density {args.density} K={K}",
-            "step": "anchor (pddp, dense+lse, mass+top-k, sparse record) + reuse (sparse+residual)",
-            "value_basis": "reuse-step sparse attention kernel time, CUDA events, mean of timed steps",
+            "step": f"anchor (pddp, dense+lse, mass+top-k, sparse record) + {R} reuse steps "
+                    "(sparse+residual, each with its own step's inputs; anchor interval "
+                    f"{R + 1})",
+            "value_basis": "reuse-step sparse attention kernel time, CUDA events, mean over the "
+                           "reuse launches of the timed steps",
             "l2": "inputs larger than L2 (0.77 GB per tensor); no flush",
             "parallelism": f"dp{world} (independent replicas)",
             "layout": "[B,N,H,D]" if layout == mcs.LAYOUT_BNHD else "[B,H,N,D]",
@@ -458,6 +468,7 @@ def run_gpu(args, w, K, rank, world, dist):
         "efficiency_vs_ideal": speedup * args.density,
         "dense_equivalent_tflops": job_tflops(world, flops_dense, t_sparse),
         "stage_ms": stage_ms,
+        "reuse_launch_ms": reuse_launch_ms,  # by position after the anchor
         "kernels": kernels,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -588,6 +599,8 @@ def main():
     ap.add_argument("--density", type=float, default=0.2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reuse-per-anchor", type=int, default=4,
+                    help="reuse steps timed after each anchor (anchor interval - 1)")
     ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"],
                     help="activation layout: [B,H,N,D] or [B,N,H,D]")
     ap.add_argument("--diagnostics", action="store_true",
