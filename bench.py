@@ -50,10 +50,9 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # while the source is unchanged).
 TRAFFIC = {
     # ncu dram bytes (read + write) of the sparse reuse launch of the 40-head
-    # large workload, one-pass capture at full size (mean of the two timed
+    # large workload, one-pass capture at full size (mean of the eight timed
     # launches of `bench.py --steps 2 --warmup 1 --no-e2e --no-cpu-baseline`)
-    "attn.cu": {"sha": "1e2afdf3b6cf",
-                "bytes_per_launch": (6478033920 + 763077376 + 6466837760 + 762905344) // 2},
+    "attn.cu": {"sha": "1e2afdf3b6cf", "bytes_per_launch": 7190463584},
 }
 
 
