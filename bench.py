@@ -194,6 +194,11 @@ def oracle_time(s, min_seconds):
     return flops / dt / 1e12, dt, desc
 
 
+def workload_label(w, density, K) -> str:
+    """The `config.workload` both arms print for the same run."""
+    return f"{w.name} B={w.B} H={w.H} N={w.N} D={w.D} C={w.C} density {density} K={K}"
+
+
 def run_reference(args, w, K, rank):
     if rank != 0:
         return
@@ -211,7 +216,7 @@ def run_reference(args, w, K, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "large video B=1 H=40 N=75600 D=128 C=128 density 0.2 K=15120",
+        "config": {"workload": workload_label(w, args.density, K),
                    "sample": "bounded sample per step"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": desc},
@@ -452,8 +457,7 @@ def run_gpu(args, w, K, rank, world, dist):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{w.name} B={w.B} H={w.H} N={w.N} D={w.D} C={w.C} "
-                        f"density {args.density} K={K}",
+            "workload": workload_label(w, args.density, K),
             "step": f"anchor (pddp, dense+lse, mass+top-k, sparse record) + {R} reuse steps "
                     "(sparse+residual, each with its own step's inputs; anchor interval "
                     f"{R + 1})",
