@@ -334,30 +334,45 @@ __global__ void __launch_bounds__(kPowThreads)
   const int tid = threadIdx.x;
   constexpr int LD = D + 1;
   const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * (D * D + D);
-  // Sum the chunks' partial moments: each thread takes 8 elements at once so
-  // that 8 independent loads per chunk are in flight (one element per thread
-  // made every load wait for the previous one).
-  constexpr int DD = D * D + D;
-  constexpr int kU = 8;
-  for (int i0 = tid; i0 < DD; i0 += kU * kPowThreads) {
-    float acc[kU];
+  // Sum the chunks' partial moments: each thread takes 4 float4 vectors at
+  // once, so that 64 bytes of independent loads per chunk are in flight (one
+  // element per thread made every load wait for the previous one).  Chunks
+  // are added in order, per element, as before.
+  constexpr int DD = D * D + D;  // a multiple of 4; chunk rows are 16-byte aligned
+  static_assert((D * D + D) % 4 == 0, "partial rows are whole float4 vectors");
+  constexpr int kU = 4;
+  const float4* base4 = reinterpret_cast<const float4*>(base);
+  for (int i0 = tid; i0 < DD / 4; i0 += kU * kPowThreads) {
+    float4 acc[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) acc[u] = 0.f;
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = 0; c < nchunks; ++c) {
-      const float* pc = base + (size_t)c * DD;
+      const float4* pc = base4 + (size_t)c * (DD / 4);
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int i = i0 + u * kPowThreads;
-        if (i < DD) acc[u] += __ldg(pc + i);
+        if (i < DD / 4) {
+          const float4 x = __ldg(pc + i);
+          acc[u].x += x.x;
+          acc[u].y += x.y;
+          acc[u].z += x.z;
+          acc[u].w += x.w;
+        }
       }
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int i = i0 + u * kPowThreads;
-      if (i < D * D)
-        cov[(i / D) * LD + (i % D)] = acc[u];
-      else if (i < DD)
-        s[i - D * D] = acc[u];
+      if (i >= DD / 4) continue;
+      const float vals[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 4 * i + e;
+        if (k < D * D)
+          cov[(k / D) * LD + (k % D)] = vals[e];
+        else
+          s[k - D * D] = vals[e];
+      }
     }
   }
   __syncthreads();
