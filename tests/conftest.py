@@ -10,4 +10,4 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size workload parity (GPU box only)")
+    config.addinivalue_line("markers", "slow: full-size workload parity (needs a GPU)")
