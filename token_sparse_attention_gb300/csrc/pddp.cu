@@ -320,78 +320,72 @@ __global__ void __launch_bounds__(kMomThreads, 2)
 
 constexpr int kPowThreads = 256;
 
+// One CTA per node.  Thread t owns row a = t / TPR of the node's covariance
+// and the contiguous columns [part*SEG, (part+1)*SEG) of it (SEG = D / TPR),
+// kept in registers for every iteration; an iteration reads only the current
+// vector from shared memory, as 16-byte broadcast loads, and sums its
+// products in four independent chains.  (Re-reading the D x D matrix from
+// shared memory every iteration made the deep tree levels, with thousands of
+// nodes, shared-memory bound.)
 template <int D>
-__global__ void __launch_bounds__(kPowThreads)
+__global__ void __launch_bounds__(kPowThreads, 2)
     pddp_power_kernel(const float* __restrict__ partials, int N, int C, int depth, int slots,
                       int max_chunks, int iters, float* __restrict__ nodevec) {
-  extern __shared__ float cov[];  // [D][D + 1]
-  __shared__ float s[D], v[D], w[D], red[kPowThreads / 32];
+  constexpr int TPR = kPowThreads / D;  // threads per row: 2 (D=128) or 4 (D=64)
+  constexpr int SEG = D / TPR;          // columns per thread: 64 or 16
+  static_assert(SEG % 4 == 0 && 32 % TPR == 0, "row segments are float4 vectors in one warp");
+  __shared__ __align__(16) float s[D];
+  __shared__ __align__(16) float v[D];
+  __shared__ float w[D], red[kPowThreads / 32];
   __shared__ int lead;
   const int slot = blockIdx.x, bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
   if ((nd.n + C - 1) / C <= 1) return;
   const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
   const int tid = threadIdx.x;
-  constexpr int LD = D + 1;
-  const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * (D * D + D);
-  // Sum the chunks' partial moments: each thread takes 4 float4 vectors at
-  // once, so that 64 bytes of independent loads per chunk are in flight (one
-  // element per thread made every load wait for the previous one).  Chunks
-  // are added in order, per element, as before.
-  constexpr int DD = D * D + D;  // a multiple of 4; chunk rows are 16-byte aligned
-  static_assert((D * D + D) % 4 == 0, "partial rows are whole float4 vectors");
-  constexpr int kU = 4;
-  const float4* base4 = reinterpret_cast<const float4*>(base);
-  for (int i0 = tid; i0 < DD / 4; i0 += kU * kPowThreads) {
-    float4 acc[kU];
+  const int a = tid / TPR, part = tid % TPR, b0 = part * SEG;
+  constexpr int DD = D * D + D;  // one chunk's partials: X^T X, then the column sums
+  const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * DD;
+  // this thread's covariance segment and (first D threads) the column sums,
+  // summed over the node's chunks in chunk order
+  float c[SEG];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < nchunks; ++c) {
-      const float4* pc = base4 + (size_t)c * (DD / 4);
+  for (int k = 0; k < SEG; ++k) c[k] = 0.f;
+  float sacc = 0.f;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const float* pc = base + (size_t)ch * DD;
+    const float4* row = reinterpret_cast<const float4*>(pc + a * D + b0);
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kPowThreads;
-        if (i < DD / 4) {
-          const float4 x = __ldg(pc + i);
-          acc[u].x += x.x;
-          acc[u].y += x.y;
-          acc[u].z += x.z;
-          acc[u].w += x.w;
-        }
-      }
+    for (int k4 = 0; k4 < SEG / 4; ++k4) {
+      const float4 x = __ldg(row + k4);
+      c[4 * k4] += x.x;
+      c[4 * k4 + 1] += x.y;
+      c[4 * k4 + 2] += x.z;
+      c[4 * k4 + 3] += x.w;
     }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = i0 + u * kPowThreads;
-      if (i >= DD / 4) continue;
-      const float vals[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = 4 * i + e;
-        if (k < D * D)
-          cov[(k / D) * LD + (k % D)] = vals[e];
-        else
-          s[k - D * D] = vals[e];
-      }
-    }
+    if (tid < D) sacc += __ldg(pc + D * D + tid);
+  }
+  if (tid < D) {
+    s[tid] = sacc;
+    v[tid] = rsqrtf(static_cast<float>(D));
   }
   __syncthreads();
   const float inv_n = 1.f / static_cast<float>(nd.n);
-  for (int i = tid; i < D * D; i += kPowThreads) {
-    const int a = i / D, b = i % D;
-    cov[a * LD + b] -= s[a] * s[b] * inv_n;
-  }
-  for (int i = tid; i < D; i += kPowThreads) v[i] = rsqrtf(static_cast<float>(D));
-  __syncthreads();
-  constexpr int TPR = kPowThreads / D;  // threads per row: 2 (D=128) or 4 (D=64)
-  const int a = tid / TPR, part = tid % TPR;
+  const float sa = s[a];
+#pragma unroll
+  for (int k = 0; k < SEG; ++k) c[k] -= sa * s[b0 + k] * inv_n;  // Cov = X^T X - s s^T / n
+  const float4* v4 = reinterpret_cast<const float4*>(v + b0);
   for (int it = 0; it < iters; ++it) {
-    float acc = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < D / TPR; ++i) {
-      const int b = i * TPR + part;
-      acc = fmaf(cov[a * LD + b], v[b], acc);
+    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k4 = 0; k4 < SEG / 4; ++k4) {
+      const float4 x = v4[k4];
+      acc4[0] = fmaf(c[4 * k4], x.x, acc4[0]);
+      acc4[1] = fmaf(c[4 * k4 + 1], x.y, acc4[1]);
+      acc4[2] = fmaf(c[4 * k4 + 2], x.z, acc4[2]);
+      acc4[3] = fmaf(c[4 * k4 + 3], x.w, acc4[3]);
     }
+    float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     float sq = (part == 0) ? acc * acc : 0.f;
@@ -633,9 +627,7 @@ cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int layout, 
   e = cudaFuncSetAttribute(pddp_moments_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            msmem);
   if (e != cudaSuccess) return e;
-  const int psmem = D * (D + 1) * (int)sizeof(float);
-  e = cudaFuncSetAttribute(pddp_power_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
-  if (e != cudaSuccess) return e;
+  const int psmem = 0;  // the power kernel's shared memory is static
 
   for (int d = 0; d < depths; ++d) {
     const int slots = 1 << d;
