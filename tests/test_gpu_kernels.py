@@ -487,3 +487,29 @@ def test_single_short_group():
     sp = orc.sparse_attention(P.f64(q[0, 0]), P.f64(k[0, 0]), P.f64(v[0, 0]), want, idx[0, 0],
                               C, orc.default_scale(D))
     P.assert_close(out[0, 0], sp, "single short group")
+
+
+def test_select_with_one_head_workspace_matches_all_heads():
+    # a workspace that holds one head's masses and histograms processes the
+    # heads one chunk at a time: same selection as one chunk of all heads
+    N, D, C, K, H = 3000, 128, 128, 700, 3
+    q, k, v = P.random_qkv(2, H, N, D, seed=61)
+    p = mcs.params(2, H, N, D, C, K)
+    qd, kd, vd = _dev(q, k, v)
+    perm = torch.empty(2, H, p.G * C, dtype=torch.int32, device="cuda")
+    mcs.mcs_group(p, qd, perm, mcs.empty_workspace(mcs.mcs_group_workspace(p)))
+    lse = torch.empty(2, H, N, dtype=torch.float32, device="cuda")
+    mcs.mcs_dense_attn(p, qd, kd, vd, torch.empty_like(qd), lse)
+    rup = lambda x: -(-x // 256) * 256  # noqa: E731
+    one_head = rup(p.G * N * 4) + rup(p.G * 1088 * 4)
+    out = {}
+    for name, nbytes in (("all", mcs.mcs_anchor_workspace(p)), ("one", one_head)):
+        idx = torch.empty(2, H, p.G, K, dtype=torch.int32, device="cuda")
+        ret = torch.empty(2, H, p.G, dtype=torch.float32, device="cuda")
+        mcs.mcs_select(p, qd, kd, lse, perm, idx, mcs.empty_workspace(nbytes), ret)
+        out[name] = (idx, ret)
+    assert mcs.mcs_device_status() == 0
+    assert torch.equal(out["all"][0], out["one"][0])
+    assert torch.equal(out["all"][1], out["one"][1])
+    with pytest.raises(mcs.McsError):  # less than one head: refused before any launch
+        mcs.mcs_select(p, qd, kd, lse, perm, out["one"][0], mcs.empty_workspace(one_head - 256))

@@ -88,11 +88,13 @@ def test_bad_layout_is_rejected_before_launch():
         mcs.mcs_dense_attn(p, q, q, q, torch.empty_like(q))
 
 
-def test_large_workload_dense_and_reuse_layout_independent():
-    # full size (40 heads of 75600 tokens), the launches the benchmark times
+@pytest.mark.parametrize("name,density", [("large", 0.2), ("asset3d", 0.15)])
+def test_full_size_dense_and_reuse_layout_independent(name, density):
+    # full size (all heads), the launches the benchmark times; D = C = 128
+    # and D = C = 64
     from token_sparse_attention_gb300 import synth
-    w = synth.workload("large")
-    K = w.K(0.2)
+    w = synth.workload(name)
+    K = w.K(density)
     q, k, v = synth.make_qkv(w, 0, device="cuda")
     p0 = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
     p1 = mcs.params(w.B, w.H, w.N, w.D, w.C, K, layout=mcs.LAYOUT_BNHD)

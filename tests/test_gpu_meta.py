@@ -160,3 +160,28 @@ def test_layer_pipeline_prefetch_one_ahead_matches_resident():
     for layer in range(L):
         np.testing.assert_array_equal(got[layer].view(torch.int16).cpu().numpy(),
                                       want[layer].view(torch.int16).cpu().numpy())
+
+
+def test_round_trip_in_bnhd_layout():
+    # the entry's residual follows the activations' layout; one copy moves it
+    w = synth.workload("tiny")
+    p = mcs.params(w.B, w.H, w.N, w.D, w.C, w.K(0.2), layout=mcs.LAYOUT_BNHD)
+    q, k, v = [t.cuda().transpose(1, 2).contiguous() for t in synth.make_qkv(w, 0)]
+    entry = torch.empty(mcs.mcs_meta_bytes(p), dtype=torch.uint8, device="cuda")
+    idx = _anchor_into(p, q, k, v, entry)
+    assert mcs.meta_views(p, entry)[2].shape == (w.B, w.N, w.H, w.D)
+    host = torch.empty_like(entry, device="cpu").pin_memory()
+    copy = torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    st = mcs.Stager(p, [entry], copy)
+    want = entry.clone()
+    st.offload(0, host, after=cur)
+    st.wait(0, cur)
+    entry.zero_()
+    st.prefetch(0, host, after=cur)
+    st.wait(0, cur)
+    back = torch.empty_like(idx)
+    mcs.mcs_meta_unpack(p, entry, back)
+    torch.cuda.synchronize()
+    st.close()
+    assert torch.equal(entry, want) and torch.equal(back, idx)
