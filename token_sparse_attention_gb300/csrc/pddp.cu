@@ -133,7 +133,8 @@ struct MomLayout {
   static constexpr int kStage = 2 * kSubBytes;
   static constexpr int kBars = 2 * kStage;
   static constexpr int kUsed = kBars + 128 + 1024;
-  static constexpr int kSmem = kUsed > 80 * 1024 ? kUsed : 80 * 1024;  // <= 2 CTAs per SM
+  // three CTAs per SM: 3 x ~67 KB of shared memory, 3 x 128 TMEM columns
+  static constexpr int kSmem = kUsed;
 };
 
 __device__ __forceinline__ float smem_x(const uint8_t* stage, int row, int col) {
@@ -147,7 +148,7 @@ __device__ __forceinline__ float smem_x(const uint8_t* stage, int row, int col) 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kMomThreads, 2)
+__global__ void __launch_bounds__(kMomThreads, 3)
     pddp_moments_kernel(const __grid_constant__ CUtensorMap tq, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, int max_chunks, float* partials,
                         unsigned* status, int layout, int H, int head0) {
