@@ -351,12 +351,13 @@ def anchor_step(q, k, v, C: int, K: int, scale, iters: int = 32):
                 residual=residual)
 
 
-def reuse_step(q, k, v, perm, idx, residual, C: int, scale):
+def reuse_step(q, k, v, perm, idx, residual, C: int, scale, groups=None):
     """Output of a reuse step for one head: the current step's sparse
     attention under the cached groups and indices, plus the cached residual
     [wisp/Residual].  Returns the exact (fp64) sum; the stored output is its
-    bf16 rounding."""
-    sparse = sparse_attention(q, k, v, perm, idx, C, scale)
+    bf16 rounding.  ``groups`` restricts the work to some groups, as in
+    ``sparse_attention`` (rows of other groups are NaN)."""
+    sparse = sparse_attention(q, k, v, perm, idx, C, scale, groups=groups)
     return sparse + np.asarray(residual, np.float64)
 
 

@@ -202,6 +202,30 @@ def test_group_mass_matches_torch_softmax_and_sums_to_group_size():
     assert math.isclose(mass.sum(), members.shape[0], rel_tol=1e-12)
 
 
+def test_group_mass_several_groups_of_one_perm():
+    """Every group of one grouping against torch's softmax rows summed over
+    that group's own members (a group read through another group's rows, or
+    through the wrong perm slots, fails), and the groups together account for
+    every query: summed over all groups the masses are the column sums of the
+    full probability matrix."""
+    N, D, C = 230, 16, 32  # 8 groups, the last one short (6 rows)
+    q, k, _ = _head(N, D, 21)
+    scale = orc.default_scale(D)
+    _, lse = orc.dense_attention(q, k, k, scale)
+    perm = orc.pddp_perm(q, C, 32)
+    G = -(-N // C)
+    P = torch.softmax(torch.from_numpy(q @ k.T * scale), dim=1).numpy()
+    total = np.zeros(N)
+    for g in range(G):
+        members = orc.group_members(perm, g, C)
+        assert members.shape[0] == (C if g < G - 1 else N - (G - 1) * C)
+        mass = orc.group_mass(q, k, lse, members, scale)
+        np.testing.assert_allclose(mass, P[members].sum(0), rtol=1e-11, atol=1e-15)
+        total += mass
+    np.testing.assert_allclose(total, P.sum(0), rtol=1e-11, atol=1e-14)
+    assert math.isclose(total.sum(), N, rel_tol=1e-12)
+
+
 def test_topk_golden_ties():
     fx = json.load(open(os.path.join(GOLDEN, "topk_ties.json")))
     for case in fx["cases"]:
@@ -269,6 +293,40 @@ def test_sparse_fixed_subset_equals_sdpa_on_subset():
     np.testing.assert_allclose(sparse, want.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_sparse_distinct_idx_per_group_equals_sdpa_per_group():
+    """Each group attends to its OWN selected keys: with a different index set
+    per group, every group's rows equal torch SDPA of those queries over that
+    group's K/V subset, written back at the group's own token rows.  Reading
+    idx[0] for every group, mixing up group and row, or scattering to perm
+    positions instead of token indices fails here."""
+    N, D, C, K = 150, 16, 32, 19  # 5 groups, the last one short (22 rows)
+    q, k, v = _head(N, D, 22)
+    scale = orc.default_scale(D)
+    rng = _rng(23)
+    G = -(-N // C)
+    perm = np.full(G * C, -1, dtype=np.int64)
+    order = rng.permutation(N)
+    for g in range(G):
+        seg = np.sort(order[g * C:(g + 1) * C])
+        perm[g * C:g * C + seg.shape[0]] = seg
+    idx = np.stack([np.sort(rng.choice(N, K, replace=False)) for _ in range(G)])
+    assert len({tuple(r) for r in idx}) == G  # the sets really differ
+    sparse = orc.sparse_attention(q, k, v, perm, idx, C, scale)
+    assert not np.any(np.isnan(sparse))
+    for g in range(G):
+        rows = perm[g * C:(g + 1) * C]
+        rows = rows[rows >= 0]
+        want = torch.nn.functional.scaled_dot_product_attention(
+            *(torch.from_numpy(a)[None, None] for a in (q[rows], k[idx[g]], v[idx[g]])),
+            scale=scale)[0, 0]
+        np.testing.assert_allclose(sparse[rows], want.numpy(), rtol=1e-10, atol=1e-12)
+    # the same groups processed one at a time agree with the whole-head call
+    for g in (0, G - 1):
+        rows = orc.group_members(perm, g, C)
+        np.testing.assert_array_equal(
+            orc.sparse_attention_group(q, k, v, rows, idx[g], scale), sparse[rows])
+
+
 def test_anchor_identity_and_reuse_reproduces_dense():
     N, D, C, K = 256, 32, 32, 40
     q, k, v = _head(N, D, 15)
@@ -283,6 +341,12 @@ def test_anchor_identity_and_reuse_reproduces_dense():
     out = orc.reuse_step(q, k, v, a["perm"], a["idx"], a["residual"], C, scale)
     assert np.max(np.abs(out - a["dense"])) < 1e-2
     assert np.max(np.abs(orc.round_to_bf16(out) - a["dense_bf16"])) <= np.max(np.abs(a["dense"])) * 2 ** -7
+    # restricted to some groups, the reuse step gives exactly those groups' rows
+    part = orc.reuse_step(q, k, v, a["perm"], a["idx"], a["residual"], C, scale, groups=[1, 6])
+    rows = np.concatenate([orc.group_members(a["perm"], g, C) for g in (1, 6)])
+    np.testing.assert_array_equal(part[rows], out[rows])
+    others = np.setdiff1d(np.arange(N), rows)
+    assert np.all(np.isnan(part[others]))
     # the selection keeps most of the mass on these peaked inputs, never more than
     # the group size
     sizes = np.array([orc.group_members(a["perm"], g, C).shape[0] for g in range(a["idx"].shape[0])])
