@@ -212,8 +212,11 @@ mcs_status mcs_anchor_select(const mcs_params* p, const void* q, const void* k, 
  * processed a batch at a time so that each batch fits the scratch.  Returns
  * MCS_ERR_WORKSPACE, launching nothing, when a single head needs more than
  * the 64 MiB (mcs_group_workspace for B = H = 1 exceeds 64 MiB).
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * Every call looks up the array's device address with the caller's device
+ * current, so a context destroyed and created again (cudaDeviceReset) is
+ * handled; the first call on each device also loads the library's kernels
+ * there, so make that first call before any stream capture.  CUDA failures
+ * return MCS_ERR_CUDA with the message in mcs_last_cuda_error().
  * All calls share the one array and nothing in it needs clearing between
  * calls; calls that overlap on the GPU (two streams, or two host threads)
  * race on it and must be serialised by the caller.

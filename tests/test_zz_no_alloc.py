@@ -54,14 +54,32 @@ def test_noalloc_matches_workspace_grouping_twice(B, H, N, D, C):
 
 
 def test_noalloc_heads_in_batches():
-    # eight heads of 32760 tokens need more than 64 MiB of scratch together,
-    # so the entry point groups them a batch at a time
+    # eight heads of 32760 tokens need more than 64 MiB of scratch together
+    # while one head fits, so the entry point groups them a batch at a time
     B, H, N, D, C = 1, 8, 32760, 128, 128
     p = mcs.params(B, H, N, D, C, 1)
     assert mcs.mcs_group_workspace(p) > (64 << 20)
+    assert mcs.mcs_group_workspace(mcs.params(1, 1, N, D, C, 1)) <= (64 << 20)
     for seed in (21, 22):
         got, want, _ = _group_both(B, H, N, D, C, seed)
         np.testing.assert_array_equal(got, want)
+
+
+def test_noalloc_leaves_device_memory_unchanged():
+    # once the library is loaded on the device (first call), a further call
+    # takes no device memory: free memory before and after is the same
+    B, H, N, D, C = 1, 4, 3000, 128, 128
+    q = P.random_qkv(B, H, N, D, 31)[0].cuda()
+    p = mcs.params(B, H, N, D, C, 1)
+    perm = torch.empty(B, H, p.G * C, dtype=torch.int32, device="cuda")
+    mcs.mcs_group_noalloc(p, q, perm)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    mcs.mcs_group_noalloc(p, q, perm)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert mcs.mcs_device_status() == 0
 
 
 def test_noalloc_refuses_oversized_problem():

@@ -1,8 +1,6 @@
 // mcs_group_noalloc: query grouping for callers that cannot allocate device
 // memory.  Its scratch is a fixed array compiled into the library instead of
 // a caller-provided workspace; see the declaration in include/mcs.h.
-#include <mutex>
-
 #include "internal.h"
 #include "mcs.h"
 
@@ -15,24 +13,16 @@ constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 // In host code `g_noalloc_scratch` only names a host-side shadow of the
-// array; kernels must be given its device address, looked up once per device.
-constexpr int kMaxDevices = 256;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
+// array; kernels must be given its device address.  The address is looked up
+// on every call, with the caller's device current: a cached address would go
+// stale if the device's context were destroyed and created again (after
+// cudaDeviceReset the module is loaded anew and the array may move).  The
+// first lookup on a device loads the library's kernels there.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -57,21 +47,23 @@ extern "C" mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int3
 
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
-  if (e != cudaSuccess) return MCS_ERR_CUDA;
+  if (e != cudaSuccess) return mcs::record_cuda_error(e, "cudaGetSymbolAddress(noalloc scratch)");
   unsigned* status = nullptr;
-  if ((e = mcs::device_status_word(&status)) != cudaSuccess) return MCS_ERR_CUDA;
+  if ((e = mcs::device_status_word(&status)) != cudaSuccess)
+    return mcs::record_cuda_error(e, "status word");
 
   // The kernels address q's rows by global head (either layout), so every
   // batch uses the one gather map over all rows.
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
   CUtensorMap tq;
-  if (!mcs::encode_gather_map(&tq, qb, static_cast<long long>(BH) * N, D)) return MCS_ERR_CUDA;
+  if (!mcs::encode_gather_map(&tq, qb, static_cast<long long>(BH) * N, D))
+    return mcs::record_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(noalloc gather)");
   for (int h0 = 0; h0 < BH; h0 += batch) {
     const int hc = BH - h0 < batch ? BH - h0 : batch;
     e = mcs::launch_pddp(qb, &tq, p->layout, p->H, h0, hc, N, D, C, iters,
                          perm + static_cast<size_t>(h0) * G * C, scratch, kNoallocScratchBytes,
                          status, stream);
-    if (e != cudaSuccess) return MCS_ERR_CUDA;
+    if (e != cudaSuccess) return mcs::record_cuda_error(e, "noalloc grouping launch");
   }
   return MCS_OK;
 }
