@@ -22,7 +22,9 @@
 //               threads copy each unit's query rows (by perm) and indexed K/V
 //               rows (by idx) with 16-byte cp.async straight into the
 //               128-byte-swizzled layout the MMA reads, and arrive on the
-//               stage's mbarrier when their copies land.
+//               stage's mbarrier when their copies land.  Each warp reads the
+//               indices of its rows of a tile once (one per lane, coalesced)
+//               and broadcasts them with shuffles.
 //   warp 15     TMEM allocation and MMA issue (one elected lane)
 // Shared memory: Q_a and Q_b (the QK A-operands) and a ring of K/V tiles.
 // TMEM (512 columns): S_a, S_b (128 fp32 columns each; P is written over S
@@ -225,13 +227,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // Sparse.  A tile is kChunks 16-byte chunks (row r = c / kSegs,
-      // segment c % kSegs); producer thread p copies chunks p, p + kPT, ...
+      // Sparse.  Q rows: a 128-row tile is kChunks 16-byte chunks (row r =
+      // c / kSegs, segment c % kSegs); producer thread p copies chunks p,
+      // p + kPT, ...  K/V tiles: each warp instruction copies kRPI whole rows
+      // (lane -> row kRPI * rg + lane / kSegs, segment lane % kSegs); producer
+      // warp pw takes the row groups rg = pw, pw + kProducers, ...  The tokens
+      // of a tile's rows are read once per warp (one index per lane) and
+      // broadcast with shuffles.
       constexpr int kPT = 32 * kProducers;
       constexpr int kSegs = D * 2 / 16;                 // 16-byte segments per row
       constexpr int kChunks = BM * kSegs;
-      constexpr int kPer = (kChunks + kPT - 1) / kPT;   // chunks per thread (at most)
+      constexpr int kPer = (kChunks + kPT - 1) / kPT;   // Q chunks per thread (at most)
+      constexpr int kRPI = 32 / kSegs;                  // rows per warp instruction
+      constexpr int kRG = BN / kRPI;                    // row groups per tile
+      constexpr int kGPW = (kRG + kProducers - 1) / kProducers;  // row groups per warp
+      static_assert(kGPW * kRPI <= 32, "one index per lane");
       const int tid = (warp - kFirstProducer) * 32 + lane;
+      const int pw = warp - kFirstProducer;
+      const int sub = lane / kSegs, seg = lane % kSegs;
       const int group[2] = {2 * pair, has_b ? 2 * pair + 1 : 2 * pair};
       bool bad = false;
       // Q rows of both units (perm order); padding slots, rows >= C and a
@@ -242,43 +255,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kPer; ++k) {
           const int c = tid + kPT * k;
           if (c < kChunks) {
-            const int r = c / kSegs, seg = c % kSegs;
+            const int r = c / kSegs, sg = c % kSegs;
             int tok = (r < a.C && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
             if (tok >= a.N) { bad = true; tok = -1; }
             const __nv_bfloat16* src =
-                a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + seg * 8;
-            cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, seg), src, tok >= 0);
+                a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + sg * 8;
+            cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, sg), src, tok >= 0);
           }
         }
       }
       cp_async_arrive(q_full);
-      // Rows (RowMap) of the tokens of this thread's chunks of tile j of
-      // unit x; loaded two tiles ahead so that the index latency (the index
-      // array is read once, from HBM) stays off the critical path.
-      auto load_rows = [&](int x, int j, int* out) {
+      // This lane's row (RowMap) of tile j of unit x: lane l < kGPW * kRPI
+      // holds the row of group pw + kProducers * (l / kRPI), sub-row l % kRPI.
+      // Loaded two tiles ahead so that the index latency (the index array is
+      // read once, from HBM) stays off the critical path.
+      auto load_rows = [&](int x, int j) -> int {
         const int32_t* idx_g = a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int c = tid + kPT * k;
-          int col = j * BN + (c < kChunks ? c / kSegs : 0);
+        int out = 0;
+        if (lane < kGPW * kRPI) {
+          const int rg = pw + kProducers * (lane / kRPI);
+          int col = j * BN + (rg < kRG ? rg * kRPI + lane % kRPI : 0);
           col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked in softmax
           int tok = __ldg(idx_g + col);
           if (tok < 0 || tok >= a.N) { bad = true; tok = 0; }
-          out[k] = rm.rbase + tok * rm.rstride;
+          out = rm.rbase + tok * rm.rstride;
         }
+        return out;
       };
       // Copy the rows of one K or V tile into the stage of ring item `it`.
-      auto copy_tile = [&](int it, const __nv_bfloat16* src, const int* rows) -> bool {
+      auto copy_tile = [&](int it, const __nv_bfloat16* src, int rows) -> bool {
         const int st = it % NS;
         if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
         uint8_t* stage = ring + st * L::kTileBytes;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int c = tid + kPT * k;
-          if (c < kChunks) {
-            const int r = c / kSegs, seg = c % kSegs;
-            cp_async16(stage + swz_offset(r, seg), src + static_cast<size_t>(rows[k]) * D + seg * 8);
-          }
+        for (int i = 0; i < kGPW; ++i) {
+          const int rg = pw + kProducers * i;
+          const int row = __shfl_sync(0xffffffffu, rows, i * kRPI + sub);
+          if (rg < kRG)
+            cp_async16(stage + swz_offset(rg * kRPI + sub, seg),
+                       src + static_cast<size_t>(row) * D + seg * 8);
         }
         cp_async_arrive(full + st);
         ++issued;
@@ -293,12 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(idx_g + off));
       }
       // rows of tiles j (V_x(j)), j+1 (K_x(j+1)) and j+2 (being fetched)
-      int r0[2][kPer], r1[2][kPer], r2[2][kPer];
-      load_rows(0, 0, r0[0]);
-      load_rows(1, 0, r0[1]);
+      int r0[2], r1[2] = {0, 0}, r2[2] = {0, 0};
+      r0[0] = load_rows(0, 0);
+      r0[1] = load_rows(1, 0);
       if (nkv > 1) {
-        load_rows(0, 1, r1[0]);
-        load_rows(1, 1, r1[1]);
+        r1[0] = load_rows(0, 1);
+        r1[1] = load_rows(1, 1);
       }
       bool ok = copy_tile(k_item(0, 0), a.k, r0[0]) && copy_tile(k_item(1, 0), a.k, r0[1]);
       for (int j = 0; ok && j < nkv; ++j) {
@@ -309,16 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // indices of tile j+2, after this step's copies: their load latency
         // then delays nothing already due
         if (j + 2 < nkv) {
-          load_rows(0, j + 2, r2[0]);
-          load_rows(1, j + 2, r2[1]);
+          r2[0] = load_rows(0, j + 2);
+          r2[1] = load_rows(1, j + 2);
         }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          r0[0][k] = r1[0][k];
-          r0[1][k] = r1[1][k];
-          r1[0][k] = r2[0][k];
-          r1[1][k] = r2[1][k];
-        }
+        r0[0] = r1[0];
+        r0[1] = r1[1];
+        r1[0] = r2[0];
+        r1[1] = r2[1];
       }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
       if (*abort_flag) asm volatile("cp.async.wait_all;" ::: "memory");  // copies land first
