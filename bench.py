@@ -76,6 +76,14 @@ def reduce_max_over_ranks(vals, dist, device):
     return t.tolist()
 
 
+def sum_over_ranks(x, dist, device):
+    """Sum of one number over all ranks (every rank gets the result)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return t.item()
+
+
 def job_tflops(world: int, flops_per_replica: float, ms: float) -> float:
     """Whole-job throughput of `world` independent replicas that each do
     flops_per_replica in `ms` (the max over ranks): weak scaling."""
@@ -229,32 +237,54 @@ def run_reference(args, w, K, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
+def rank_heads(w, rank, world, split):
+    """The problem a rank works on and the flattened heads it owns.
+
+    weak:   the job is `world` copies of the workload's batch (global batch
+            world * B); rank r owns flattened heads [r*B*H, (r+1)*B*H), so
+            every rank's work equals the single-GPU workload.
+    strong: the job is the workload itself; its B*H heads are split into
+            contiguous ranges (shard.head_range).
+    Returns (global workload, start, stop)."""
+    from token_sparse_attention_gb300 import shard
+
+    wg = dataclasses.replace(w, B=w.B * world) if split == "weak" else w
+    h0, h1 = shard.head_range(rank, world, wg.B * wg.H)
+    return wg, h0, h1
+
+
 def run_gpu(args, w, K, rank, world, dist):
     from token_sparse_attention_gb300 import mcs
 
     mcs.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
     layout = mcs.LAYOUT_BNHD if args.layout == "bnhd" else mcs.LAYOUT_BHND
-    p = mcs.params(w.B, w.H, w.N, w.D, w.C, K, layout=layout)
-    G = p.G
-    BH = w.B * w.H
+    wg, h0, h1 = rank_heads(w, rank, world, args.split)
+    heads = list(range(h0, h1))
 
     def lay(t):  # the generator writes [B,H,N,D]; DiT blocks hold [B,N,H,D]
         return t.transpose(1, 2).contiguous() if layout == mcs.LAYOUT_BNHD else t
 
-    q0, k0, v0 = (lay(t) for t in synth.make_qkv(w, 0, device=dev))
+    # this rank's heads only: [B, H, N, D] when it owns the whole batch,
+    # else one batch of h1 - h0 heads
+    q0, k0, v0 = (lay(t) for t in synth.make_qkv(wg, 0, heads=heads, device=dev))
+    Bl, Hl = (q0.shape[0], q0.shape[2]) if layout == mcs.LAYOUT_BNHD else q0.shape[:2]
+    p = mcs.params(Bl, Hl, w.N, w.D, w.C, K, layout=layout)
+    G = p.G
+    BH = Bl * Hl
     # the anchor's metadata serves the next R denoising steps, each with its
     # own inputs (the generator's steps 1..R)
     R = args.reuse_per_anchor
-    reuse_in = [tuple(lay(t) for t in synth.make_qkv(w, s_, device=dev)) for s_ in range(1, R + 1)]
+    reuse_in = [tuple(lay(t) for t in synth.make_qkv(wg, s_, heads=heads, device=dev))
+                for s_ in range(1, R + 1)]
     q1, k1, v1 = reuse_in[0]
-    perm = torch.empty(w.B, w.H, G * w.C, dtype=torch.int32, device=dev)
-    idx = torch.empty(w.B, w.H, G, K, dtype=torch.int32, device=dev)
+    perm = torch.empty(Bl, Hl, G * w.C, dtype=torch.int32, device=dev)
+    idx = torch.empty(Bl, Hl, G, K, dtype=torch.int32, device=dev)
     dense = torch.empty_like(q0)
-    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    lse = torch.empty(Bl, Hl, w.N, dtype=torch.float32, device=dev)
     res = torch.empty_like(q0)
     out = torch.empty_like(q0)
-    retained = torch.empty(w.B, w.H, G, dtype=torch.float32, device=dev)
+    retained = torch.empty(Bl, Hl, G, dtype=torch.float32, device=dev)
     ws_bytes = mcs.mcs_anchor_workspace(p)
     ws = mcs.empty_workspace(ws_bytes, dev)
     stream = torch.cuda.current_stream()
@@ -399,16 +429,21 @@ def run_gpu(args, w, K, rank, world, dist):
         if mcs.mcs_device_status() != 0:
             raise RuntimeError("device status after the end-to-end runs")
 
-    # ---- max over ranks
+    # ---- max over ranks; FLOPs summed over ranks (head ranges may differ by one)
     total_ms, t_sparse, t_dense, e2e_ms, staged_ms = reduce_max_over_ranks(
         [total_ms, stage_ms["reuse"], stage_ms["dense"], e2e["ms"] if e2e else 0.0,
          staging["ms"] if staging else 0.0], dist, dev)
+    job_heads = sum_over_ranks(BH, dist, dev)
+    extra = None
+    if world == 1 and not args.no_workloads:
+        extra = run_schedules(dev)
     if rank != 0:
         return
 
-    flops_sparse = 4.0 * BH * w.N * K * w.D
+    flops_sparse = 4.0 * BH * w.N * K * w.D  # this rank's heads
     flops_dense = 4.0 * BH * w.N * w.N * w.D
-    value = job_tflops(world, flops_sparse, t_sparse)
+    job_flops_sparse = 4.0 * job_heads * w.N * K * w.D
+    value = job_flops_sparse / (t_sparse * 1e-3) / 1e12
     speedup = t_dense / t_sparse
     peaks, peak_kind = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -452,7 +487,7 @@ def run_gpu(args, w, K, rank, world, dist):
         "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": args.split,
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
@@ -464,12 +499,16 @@ def run_gpu(args, w, K, rank, world, dist):
             "value_basis": "reuse-step sparse attention kernel time, CUDA events, mean over the "
                            "reuse launches of the timed steps",
             "l2": "inputs larger than L2 (0.77 GB per tensor); no flush",
-            "parallelism": f"dp{world} (independent replicas)",
+            "parallelism": (f"heads{world}: each rank owns a contiguous range of the "
+                            f"flattened heads ({args.split} scaling: "
+                            + ("global batch = ranks x the workload's batch"
+                               if args.split == "weak" else "the workload's heads split")
+                            + "); no collective on the data path"),
             "layout": "[B,N,H,D]" if layout == mcs.LAYOUT_BNHD else "[B,H,N,D]",
         },
         "speedup_vs_dense": speedup,
         "efficiency_vs_ideal": speedup * args.density,
-        "dense_equivalent_tflops": job_tflops(world, flops_dense, t_sparse),
+        "dense_equivalent_tflops": job_flops_sparse / K * w.N / (t_sparse * 1e-3) / 1e12,
         "stage_ms": stage_ms,
         "reuse_launch_ms": reuse_launch_ms,  # by position after the anchor
         "kernels": kernels,
@@ -478,7 +517,7 @@ def run_gpu(args, w, K, rank, world, dist):
                      "kernel": "token-sparse attention (reuse step)",
                      "peak_source": f"bf16_tflops_sustained ({peak_kind})"},
         "cpu_baseline": cpu,
-        "e2e": ({"value": job_tflops(world, flops_sparse, e2e_ms), "unit": "TFLOP/s",
+        "e2e": ({"value": job_flops_sparse / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                  "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                  "ms_per_step": e2e_ms,
                  "pipelining": "step i+1's host->device copies and step i-1's "
@@ -497,7 +536,120 @@ def run_gpu(args, w, K, rank, world, dist):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
+    if extra is not None:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
+
+
+# The workloads' denoising schedules (single GPU), each density measured on its
+# own: (workload, density, timed passes over the schedule).
+SCHEDULES = [("small", 0.1, 3), ("small", 0.2, 3), ("small", 0.3, 3),
+             ("long", 0.15, 2), ("long", 0.25, 2), ("asset3d", 0.15, 3)]
+
+
+def schedule_pass(p, steps, anchors, inputs, bufs, stream):
+    """One pass over a denoising schedule: an anchor step (grouping, dense
+    attention + LSE, exact selection, sparse attention recording the
+    residual) at each anchor, a reuse step (sparse attention + cached
+    residual) otherwise, each on its own step's inputs.  Returns the events
+    bracketing every stage, in order."""
+    from token_sparse_attention_gb300 import mcs
+
+    perm, idx, dense, lse, res, out, retained, ws = bufs
+    marks = []
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        marks.append((name, e))
+
+    mark("start")
+    for t in range(steps):
+        q, k, v = inputs[t]
+        if t in anchors:
+            mcs.mcs_group(p, q, perm, ws)
+            mark("pddp")
+            mcs.mcs_dense_attn(p, q, k, v, dense, lse)
+            mark("dense")
+            mcs.mcs_select(p, q, k, lse, perm, idx, ws, retained)
+            mark("select")
+            mcs.mcs_sparse_attn_record(p, q, k, v, perm, idx, dense, res)
+            mark("record")
+        else:
+            mcs.mcs_sparse_attn(p, q, k, v, perm, idx, res, out)
+            mark("reuse")
+    return marks
+
+
+def run_schedules(dev):
+    """Per-workload measurements: each workload's schedule (anchors and reuse
+    steps on drifting inputs) timed stage by stage with CUDA events.  Reports
+    the reuse-step sparse kernel (effective TFLOP/s, speedup over this
+    library's dense kernel on the same workload, efficiency against the ideal
+    1/density, fraction of the measured sustained bf16 peak), the anchor's
+    cost, and the schedule's time per step with the density it amounts to:
+    equivalent density = time per step / dense attention time; the anchors'
+    share of it, anchor_delta_s = anchors x (anchor step - reuse step) /
+    (steps x dense), is what the pages express as points of density."""
+    from token_sparse_attention_gb300 import mcs
+
+    peaks, _ = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    stream = torch.cuda.current_stream()
+    res_all = {}
+    for name, density, reps in SCHEDULES:
+        w = synth.workload(name)
+        K = w.K(density)
+        p = mcs.params(w.B, w.H, w.N, w.D, w.C, K)
+        G = p.G
+        inputs = [synth.make_qkv(w, t, device=dev) for t in range(w.steps)]
+        q0 = inputs[0][0]
+        bufs = (torch.empty(w.B, w.H, G * w.C, dtype=torch.int32, device=dev),
+                torch.empty(w.B, w.H, G, K, dtype=torch.int32, device=dev),
+                torch.empty_like(q0), torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev),
+                torch.empty_like(q0), torch.empty_like(q0),
+                torch.empty(w.B, w.H, G, dtype=torch.float32, device=dev),
+                mcs.empty_workspace(mcs.mcs_anchor_workspace(p), dev))
+        schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream)  # warm-up
+        torch.cuda.synchronize()
+        per = {}
+        for _ in range(reps):
+            marks = schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream)
+            torch.cuda.synchronize()
+            for (_, a), (n, b) in zip(marks, marks[1:]):
+                per.setdefault(n, []).append(a.elapsed_time(b))
+        if mcs.mcs_device_status() != 0:
+            raise RuntimeError(f"device status after the {name} schedule")
+        n_anchor, n_reuse = len(w.anchors), w.steps - len(w.anchors)
+        stage = {n: statistics.mean(v) for n, v in per.items()}
+        anchor_ms = sum(stage[n] for n in ("pddp", "dense", "select", "record"))
+        reuse_ms = stage["reuse"]
+        total = sum(sum(v) for v in per.values()) / reps
+        BH = w.B * w.H
+        fl_sparse = 4.0 * BH * w.N * K * w.D
+        tfl = fl_sparse / (reuse_ms * 1e-3) / 1e12
+        speedup = stage["dense"] / reuse_ms
+        res_all[f"{name} s={density}"] = {
+            "workload": workload_label(w, density, K),
+            "schedule": f"{w.steps} steps, anchors at {list(w.anchors)}, drift {w.drift} per step",
+            "sparse_reuse_ms": reuse_ms,
+            "sparse_tflops": tfl,
+            "dense_ms": stage["dense"],
+            "dense_tflops": 4.0 * BH * w.N * w.N * w.D / (stage["dense"] * 1e-3) / 1e12,
+            "speedup_vs_dense": speedup,
+            "efficiency_vs_ideal": speedup * density,
+            "roofline_frac": tfl / peak,
+            "anchor_ms": anchor_ms,
+            "anchor_stage_ms": {n: stage[n] for n in ("pddp", "dense", "select", "record")},
+            "ms_per_step": total / w.steps,
+            "equivalent_density": total / w.steps / stage["dense"],
+            "anchor_delta_s": n_anchor * (anchor_ms - reuse_ms) / (w.steps * stage["dense"]),
+            "passes": reps,
+            "n_anchor": n_anchor, "n_reuse": n_reuse,
+        }
+        del inputs, bufs, q0
+        torch.cuda.empty_cache()
+    return res_all
 
 
 def run_diagnostics(args, w):
@@ -608,6 +760,11 @@ def main():
                     help="activation layout: [B,H,N,D] or [B,N,H,D]")
     ap.add_argument("--diagnostics", action="store_true",
                     help="print the selector diagnostics line instead of the bench line")
+    ap.add_argument("--split", default="weak", choices=["weak", "strong"],
+                    help="several GPUs: weak = each rank a full copy of the workload's heads "
+                         "(global batch grows), strong = the workload's heads split over ranks")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload schedule measurements (single GPU only)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (smaller cases for profiling; not a bench number)")
     args = ap.parse_args()
