@@ -17,9 +17,11 @@
 // position) moves, nodes being contiguous position ranges.
 //
 // One depth = four launches:
-//   pddp_moments   per (head, node, chunk of <= kChunkRows rows): X^T X and
-//                  sum x of the chunk's rows on tcgen05 (A = X^T, B = X, both
-//                  MN-major views of the same gathered tile), fp32 in TMEM
+//   pddp_moments   per (head, node, chunk of <= kChunkRows rows): the rows,
+//                  gathered in position order with 16-byte cp.async into a
+//                  swizzled two-stage ring; X^T X on tcgen05 (A = X^T, B = X,
+//                  both MN-major views of the same tile), fp32 in TMEM; the
+//                  column sums on the CUDA cores (16-byte shared loads)
 //   pddp_power     per (head, node): sum the chunk partials in fixed order,
 //                  Cov = X^T X - s s^T / n, then `iters` steps v <- Cov v/|Cov v|
 //                  from (1,..,1)/sqrt(D); sign: largest |v_d| positive
@@ -35,7 +37,9 @@ namespace mcs {
 namespace {
 
 constexpr int kChunkRows = 1024;  // rows per moments CTA (8 tiles of 128)
-constexpr int kMomThreads = 192;
+constexpr int kMomProducers = 4;  // cp.async producer warps of the moments kernel
+constexpr int kMomMmaWarp = 4 + kMomProducers;
+constexpr int kMomThreads = 32 * (kMomMmaWarp + 1);
 
 struct Node {
   int start, n;
@@ -133,23 +137,18 @@ struct MomLayout {
   static constexpr int kStage = 2 * kSubBytes;
   static constexpr int kBars = 2 * kStage;
   static constexpr int kUsed = kBars + 128 + 1024;
-  // three CTAs per SM: 3 x ~67 KB of shared memory, 3 x 128 TMEM columns
   static constexpr int kSmem = kUsed;
 };
 
-__device__ __forceinline__ float smem_x(const uint8_t* stage, int row, int col) {
-  // element (row, col) of a 128B-swizzled tile pair
-  const int sub = col >> 6;
-  const int c = col & 63;
-  const int chunk = (c >> 3) ^ (row & 7);
-  const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(
-      stage + sub * (128 * 128) + row * 128 + chunk * 16 + (c & 7) * 2);
-  return __bfloat162float(*p);
+// Byte offset of 16-byte chunk `seg` of row r in a stage of two 128-byte-
+// swizzled sub-tiles [128 rows x 128 B] (columns 0-63, 64-127).
+__device__ __forceinline__ int mom_swz(int r, int seg) {
+  return (seg >> 3) * (128 * 128) + r * 128 + (((seg & 7) ^ (r & 7)) << 4);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kMomThreads, 3)
-    pddp_moments_kernel(const __grid_constant__ CUtensorMap tq, const int32_t* __restrict__ perm,
+    pddp_moments_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, int max_chunks, float* partials,
                         unsigned* status, int layout, int H, int head0) {
   using L = MomLayout<D>;
@@ -157,9 +156,9 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint64_t* full = bars + 0;   // [2]
-  uint64_t* ready = bars + 2;  // [2]
-  uint64_t* empty = bars + 4;  // [2]
+  uint64_t* full = bars + 0;   // [2] rows landed (every producer thread)
+  uint64_t* ready = bars + 2;  // [2] column sums taken (4 warp arrivals)
+  uint64_t* empty = bars + 4;  // [2] MMA done with the stage
   uint64_t* done = bars + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -173,7 +172,7 @@ __global__ void __launch_bounds__(kMomThreads, 3)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(full + s, 1);
+      mbar_init(full + s, kMomProducers * 32);
       mbar_init(ready + s, 4);
       mbar_init(empty + s, 1);
     }
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(kMomThreads, 3)
     }
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  if (warp == kMomMmaWarp) {
     tmem_alloc(tmem_slot, 128);
     tmem_relinquish();
   }
@@ -200,40 +199,40 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   const int32_t* pos = perm + (size_t)bh * N + nd.start + chunk * kChunkRows;
   const RowMap rm = row_map(layout, H, N, head0 + bh);  // rows of q in either layout
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp >= 4 && warp < kMomMmaWarp) {
+    // ------------------------------------------------------------ producers
+    // Producer warp pw copies rows 32 pw .. 32 pw + 31 of each tile with
+    // 16-byte cp.async (kRPI whole rows per warp instruction, written in the
+    // swizzled layout); lane l reads the token of row 32 pw + l once and
+    // broadcasts it.  Rows past the node end are zero-filled.
+    constexpr int kSegs = D * 2 / 16;  // 16-byte segments per row
+    constexpr int kRPI = 32 / kSegs;   // rows per warp instruction
+    const int pw = warp - 4;
+    const int sub = lane / kSegs, seg = lane % kSegs;
     bool bad = false;
-    int issued = 0;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
-      int r[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rr = j * 128 + 4 * lane + i;
-        int t = rr < rows ? __ldg(pos + rr) : 0;
-        if (t < 0 || t >= N) { bad = true; t = 0; }
-        r[i] = rm.rbase + t * rm.rstride;
-      }
+      const int rr = j * 128 + pw * 32 + lane;
+      int t = rr < rows ? __ldg(pos + rr) : -1;
+      if (t >= N || (rr < rows && t < 0)) { bad = true; t = -1; }
+      const int myrow = t < 0 ? -1 : rm.rbase + t * rm.rstride;
       if (j >= 2) {
         bool ok = mbar_wait(empty + st, ((j >> 1) - 1) & 1, abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
-      if (lane == 0) mbar_expect_tx(full + st, (D / 64) * L::kSubBytes);
-      __syncwarp();
-      for (int s = 0; s < D / 64; ++s)
-        tma_gather4(smem + st * L::kStage + s * L::kSubBytes + lane * 4 * 128, &tq, s * 64, r[0],
-                    r[1], r[2], r[3], full + st);
-      ++issued;
+      uint8_t* stage = smem + st * L::kStage;
+#pragma unroll
+      for (int i = 0; i < 32 / kRPI; ++i) {
+        const int row = __shfl_sync(0xffffffffu, myrow, i * kRPI + sub);
+        const int r = pw * 32 + i * kRPI + sub;
+        cp_async16_zfill(stage + mom_swz(r, seg),
+                         q + (size_t)(row < 0 ? 0 : row) * D + seg * 8, row >= 0);
+      }
+      cp_async_arrive(full + st);
     }
     if (bad) atomicOr(status, DEV_BOUNDS);
-    if (*abort_flag && lane == 0) {
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(full + (j & 1), (j >> 1) & 1))
-          if (clock64() - t0 > kWaitLimitCycles) break;
-      }
-    }
-  } else if (warp == 5) {
+    asm volatile("cp.async.wait_all;" ::: "memory");  // every copy lands before exit
+  } else if (warp == kMomMmaWarp) {
     // ------------------------------------------------------------ MMA
     // whole warp in the loop, one elected lane issues (a lane-0-only branch
     // issues MMAs much more slowly)
@@ -242,6 +241,7 @@ __global__ void __launch_bounds__(kMomThreads, 3)
       const int st = j & 1;
       const bool ok = mbar_wait(ready + st, (j >> 1) & 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) break;
+      fence_proxy_async_smem();  // rows written by cp.async, read by the MMA
       tc_fence_after();
       const uint32_t base = smem_u32(smem + st * L::kStage);
       if (elect_one()) {
@@ -259,39 +259,58 @@ __global__ void __launch_bounds__(kMomThreads, 3)
     while (!mbar_try_wait(done, 0))
       if (clock64() - t0 > kWaitLimitCycles) break;
   } else {
-    // ------------------------------------------------------------ row sums, tails, epilogue
+    // ------------------------------------------------------------ column sums, epilogue
+    // Thread t sums the 16-byte chunk cc = t % kCC (8 columns) over the rows
+    // of row group t / kCC of every tile (rows past the node end are zero);
+    // the row groups' partial sums are added at the end.
+    constexpr int kCC = D / 8;        // 16-byte chunks per row
+    constexpr int kRG = 128 / kCC;    // row groups
+    constexpr int kRPG = 128 / kRG;   // rows per group
     const int t = threadIdx.x;  // 0..127
-    float colsum = 0.f;
+    const int cc = t % kCC, rgp = t / kCC;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       bool w = mbar_wait(full + st, (j >> 1) & 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      uint8_t* stage = smem + st * L::kStage;
-      const int valid = min(128, rows - j * 128);
-      if (valid < 128) {
-        // rows past the node end were gathered from row 0: zero them
-        for (int i = t; i < (128 - valid) * 8 * (D / 64); i += 128) {
-          const int r = valid + i / (8 * (D / 64));
-          const int rem = i % (8 * (D / 64));
-          const int s = rem / 8, c16 = rem % 8;
-          *reinterpret_cast<uint4*>(stage + s * L::kSubBytes + r * 128 + c16 * 16) =
-              make_uint4(0, 0, 0, 0);
+      const uint8_t* stage = smem + st * L::kStage;
+#pragma unroll 4
+      for (int i = 0; i < kRPG; ++i) {
+        const int r = rgp * kRPG + i;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + mom_swz(r, cc));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          acc[2 * e] += f.x;
+          acc[2 * e + 1] += f.y;
         }
-        fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-      }
-      if (t < D) {
-        for (int r = 0; r < valid; ++r) colsum += smem_x(stage, r, t);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ready + st);
-      // the producer may overwrite this stage only after the MMA's commit,
+      // the producers may overwrite this stage only after the MMA's commit,
       // which follows every compute warp's arrival
     }
+    // partial column sums of the row groups -> shared memory (the first
+    // stage: every copy into it has landed and the MMA reads it no more
+    // once `done` completes), summed below in row-group order
+    float colsum = 0.f;
     if (ok) {
       bool w = mbar_wait(done, 0, abort_flag, status);
       ok = __all_sync(0xffffffffu, w);
+    }
+    float* red = reinterpret_cast<float*>(smem);
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3: stage 0 free of readers
+    if (ok) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) red[rgp * D + cc * 8 + e] = acc[e];
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ok && t < D) {
+      for (int g = 0; g < kRG; ++g) colsum += red[g * D + t];
     }
     if (ok) {
       tc_fence_after();
@@ -303,8 +322,11 @@ __global__ void __launch_bounds__(kMomThreads, 3)
         tmem_ld32(tmem + lane_off + c * 32, v);
         tmem_ld_wait();
         if (t < D) {
+          float4* o4 = reinterpret_cast<float4*>(out + t * D + c * 32);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[t * D + c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 8; ++i)
+            o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
       }
       if (t < D) out[D * D + t] = colsum;
@@ -314,7 +336,7 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 128);
+  if (warp == kMomMmaWarp) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------- power iteration
@@ -323,87 +345,120 @@ constexpr int kPowThreads = 256;
 
 // One CTA per node.  Thread t owns row a = t / TPR of the node's covariance
 // and the contiguous columns [part*SEG, (part+1)*SEG) of it (SEG = D / TPR),
-// kept in registers for every iteration; an iteration reads only the current
-// vector from shared memory, as 16-byte broadcast loads, and sums its
-// products in four independent chains.  (Re-reading the D x D matrix from
-// shared memory every iteration made the deep tree levels, with thousands of
-// nodes, shared-memory bound.)
+// kept in registers as packed fp32 pairs for every iteration; an iteration
+// reads only the current vector from shared memory (16-byte broadcast loads)
+// and multiplies with packed f32x2 FMAs.  The matrix is first divided by its
+// trace (largest eigenvalue <= 1, so the iterate cannot overflow), and the
+// iterate is normalised after the first step, every kNormEvery steps and at
+// the end instead of every step: power iteration's direction does not depend
+// on the scale of the iterate, and a node whose covariance sends the start
+// vector to zero is caught at the first step (it keeps the start vector).
+// One block barrier per step.  (Re-reading the D x D matrix from shared
+// memory every iteration made the deep tree levels, with thousands of nodes,
+// shared-memory bound.)
 template <int D>
 __global__ void __launch_bounds__(kPowThreads, 2)
     pddp_power_kernel(const float* __restrict__ partials, int N, int C, int depth, int slots,
                       int max_chunks, int iters, float* __restrict__ nodevec) {
   constexpr int TPR = kPowThreads / D;  // threads per row: 2 (D=128) or 4 (D=64)
   constexpr int SEG = D / TPR;          // columns per thread: 64 or 16
+  constexpr int kNormEvery = 8;
   static_assert(SEG % 4 == 0 && 32 % TPR == 0, "row segments are float4 vectors in one warp");
   __shared__ __align__(16) float s[D];
-  __shared__ __align__(16) float v[D];
-  __shared__ float w[D], red[kPowThreads / 32];
+  __shared__ __align__(16) float vb[2][D];  // the iterate, double-buffered
+  __shared__ float red[kPowThreads / 32];
   __shared__ int lead;
   const int slot = blockIdx.x, bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
   if ((nd.n + C - 1) / C <= 1) return;
   const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int a = tid / TPR, part = tid % TPR, b0 = part * SEG;
   constexpr int DD = D * D + D;  // one chunk's partials: X^T X, then the column sums
   const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * DD;
-  // this thread's covariance segment and (first D threads) the column sums,
-  // summed over the node's chunks in chunk order
-  float c[SEG];
+  // this thread's covariance segment (packed pairs) and (first D threads)
+  // the column sums, summed over the node's chunks in chunk order
+  uint64_t cp[SEG / 2];
 #pragma unroll
-  for (int k = 0; k < SEG; ++k) c[k] = 0.f;
-  float sacc = 0.f;
+  for (int k = 0; k < SEG / 2; ++k) cp[k] = 0ull;
+  float sacc = 0.f, dacc = 0.f;
   for (int ch = 0; ch < nchunks; ++ch) {
     const float* pc = base + (size_t)ch * DD;
-    const float4* row = reinterpret_cast<const float4*>(pc + a * D + b0);
+    const ulonglong2* row = reinterpret_cast<const ulonglong2*>(pc + a * D + b0);
 #pragma unroll
     for (int k4 = 0; k4 < SEG / 4; ++k4) {
-      const float4 x = __ldg(row + k4);
-      c[4 * k4] += x.x;
-      c[4 * k4 + 1] += x.y;
-      c[4 * k4 + 2] += x.z;
-      c[4 * k4 + 3] += x.w;
+      const ulonglong2 x = __ldg(row + k4);
+      cp[2 * k4] = f2_add(cp[2 * k4], x.x);
+      cp[2 * k4 + 1] = f2_add(cp[2 * k4 + 1], x.y);
     }
     if (tid < D) sacc += __ldg(pc + D * D + tid);
+    if (part == 0) dacc += __ldg(pc + a * D + a);  // the diagonal, for the trace
   }
   if (tid < D) {
     s[tid] = sacc;
-    v[tid] = rsqrtf(static_cast<float>(D));
+    vb[0][tid] = rsqrtf(static_cast<float>(D));
   }
   __syncthreads();
   const float inv_n = 1.f / static_cast<float>(nd.n);
-  const float sa = s[a];
+  const float sa = s[a] * inv_n;
+  const uint64_t nsa = f2_pack(-sa, -sa);
 #pragma unroll
-  for (int k = 0; k < SEG; ++k) c[k] -= sa * s[b0 + k] * inv_n;  // Cov = X^T X - s s^T / n
-  const float4* v4 = reinterpret_cast<const float4*>(v + b0);
+  for (int k = 0; k < SEG / 2; ++k)
+    cp[k] = f2_fma(nsa, f2_pack(s[b0 + 2 * k], s[b0 + 2 * k + 1]), cp[k]);  // Cov = X^T X - s s^T / n
+  float diag = part == 0 ? dacc - sa * s[a] : 0.f;
+  // trace of Cov, then Cov / trace
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) diag += __shfl_xor_sync(0xffffffffu, diag, o);
+  if (lane == 0) red[wid] = diag;
+  __syncthreads();
+  float tr = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPowThreads / 32; ++i) tr += red[i];
+  const float inv_tr = tr > 0.f ? 1.f / tr : 1.f;
+  const uint64_t itr2 = f2_pack(inv_tr, inv_tr);
+#pragma unroll
+  for (int k = 0; k < SEG / 2; ++k) cp[k] = f2_fma(cp[k], itr2, 0ull);
+  int cur = 0;
   for (int it = 0; it < iters; ++it) {
-    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+    const ulonglong2* v2 = reinterpret_cast<const ulonglong2*>(vb[cur] + b0);
 #pragma unroll
     for (int k4 = 0; k4 < SEG / 4; ++k4) {
-      const float4 x = v4[k4];
-      acc4[0] = fmaf(c[4 * k4], x.x, acc4[0]);
-      acc4[1] = fmaf(c[4 * k4 + 1], x.y, acc4[1]);
-      acc4[2] = fmaf(c[4 * k4 + 2], x.z, acc4[2]);
-      acc4[3] = fmaf(c[4 * k4 + 3], x.w, acc4[3]);
+      const ulonglong2 x = v2[k4];
+      acc0 = f2_fma(cp[2 * k4], x.x, acc0);
+      acc1 = f2_fma(cp[2 * k4 + 1], x.y, acc1);
     }
-    float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+    float a0, a1, a2, a3;
+    f2_unpack(acc0, a0, a1);
+    f2_unpack(acc1, a2, a3);
+    float acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    float sq = (part == 0) ? acc * acc : 0.f;
-    if (part == 0) w[a] = acc;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if ((tid & 31) == 0) red[tid >> 5] = sq;
+    if (part == 0) vb[cur ^ 1][a] = acc;
     __syncthreads();
-    float norm2 = 0.f;
+    cur ^= 1;
+    if (it == 0 || (it + 1) % kNormEvery == 0 || it == iters - 1) {
+      const float x = tid < D ? vb[cur][tid] : 0.f;
+      float sq = x * x;
 #pragma unroll
-    for (int i = 0; i < kPowThreads / 32; ++i) norm2 += red[i];
-    if (norm2 == 0.f) break;  // uniform: every thread sums the same values
-    const float nrm = sqrtf(norm2);
-    if (tid < D) v[tid] = w[tid] / nrm;
-    __syncthreads();
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      __syncthreads();  // every thread has read red[] of the trace step or of the last norm
+      if (lane == 0) red[wid] = sq;
+      __syncthreads();
+      float norm2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPowThreads / 32; ++i) norm2 += red[i];
+      if (norm2 == 0.f) {  // uniform: C v = 0, keep the previous vector
+        cur ^= 1;
+        break;
+      }
+      const float inv = rsqrtf(norm2);
+      if (tid < D) vb[cur][tid] = x * inv;
+      __syncthreads();
+    }
   }
   __syncthreads();
+  const float* v = vb[cur];
   if (tid == 0) {
     int best = 0;
     float bv = fabsf(v[0]);
@@ -422,51 +477,115 @@ __global__ void __launch_bounds__(kPowThreads, 2)
 
 // ---------------------------------------------------------------- projection
 
+constexpr int kProjThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+constexpr int proj_smem_bytes() { return (kProjThreads / 32) * 32 * D * 2; }
+
+// One warp per 32 consecutive positions of a head.  The warp copies its 32
+// rows into shared memory with 16-byte cp.async (all loads in flight at
+// once), then lane l takes elements [l*E, (l+1)*E) of every row, forms its
+// partial (x - mu).v for all 32 rows with the node's mean and direction in
+// registers, and a butterfly transpose reduction leaves row l's projection
+// in lane l.
+template <int D>
+__global__ void __launch_bounds__(kProjThreads)
     pddp_project_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, const float* __restrict__ nodevec,
                         uint64_t* __restrict__ keys, int layout, int H, int head0) {
-  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  constexpr int E = D / 32;          // elements of a row per lane: 4 (D = 128) or 2 (D = 64)
+  constexpr int kSegs = D * 2 / 16;  // 16-byte chunks per row
+  static_assert(E == 2 || E == 4, "D must be 64 or 128");
+  extern __shared__ __align__(16) uint8_t proj_smem[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int p0 = (blockIdx.x * (kProjThreads / 32) + wid) * 32;
   const int bh = blockIdx.y;
-  if (p >= N) return;
-  // find the node holding position p
-  Node nd{0, N};
-  int slot = 0;
-  for (int b = 0; b < depth; ++b) {
-    const int g = (nd.n + C - 1) / C;
-    if (g <= 1) return;  // leaf: nothing to project
-    const int nl = C * (g / 2);
-    if (p - nd.start < nl) {
-      nd.n = nl;
-      slot = slot << 1;
-    } else {
-      nd.start += nl;
-      nd.n -= nl;
-      slot = (slot << 1) | 1;
+  if (p0 >= N) return;  // whole warp
+  uint8_t* buf = proj_smem + wid * 32 * D * 2;
+  const int p = p0 + lane;
+  // node holding position p; -1 for positions past N and for leaves
+  int slot = -1;
+  if (p < N) {
+    Node nd{0, N};
+    int s = 0;
+    bool leaf = false;
+    for (int b = 0; b < depth; ++b) {
+      const int g = (nd.n + C - 1) / C;
+      if (g <= 1) { leaf = true; break; }
+      const int nl = C * (g / 2);
+      if (p - nd.start < nl) {
+        nd.n = nl;
+        s = s << 1;
+      } else {
+        nd.start += nl;
+        nd.n -= nl;
+        s = (s << 1) | 1;
+      }
     }
+    if (!leaf && (nd.n + C - 1) / C > 1) slot = s;
   }
-  if ((nd.n + C - 1) / C <= 1) return;
-  const int token = perm[(size_t)bh * N + p];
-  const float* vec = nodevec + (size_t)(bh * slots + slot) * 2 * D;
+  const int token = slot >= 0 ? perm[(size_t)bh * N + p] : -1;
   const RowMap rm = row_map(layout, H, N, head0 + bh);
-  const uint4* row = reinterpret_cast<const uint4*>(q + (size_t)(rm.rbase + token * rm.rstride) * D);
-  float t = 0.f;
+  const int myrow = token >= 0 ? rm.rbase + token * rm.rstride : -1;
+  // rows -> shared memory: chunk c = lane + 32 i is segment c % kSegs of row c / kSegs
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 w = __ldg(row + c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+  for (int i = 0; i < kSegs; ++i) {
+    const int c = lane + 32 * i;
+    const int r = c / kSegs, sg = c % kSegs;
+    const int row = __shfl_sync(0xffffffffu, myrow, r);
+    cp_async16_zfill(buf + r * D * 2 + sg * 16, q + (size_t)(row < 0 ? 0 : row) * D + sg * 8,
+                     row >= 0);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncwarp();
+  float acc[32];
+  int cached = -1;
+  float vs[E], ms[E];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      const int d = c * 8 + 2 * e;
-      t = fmaf(f.x - __ldg(vec + D + d), __ldg(vec + d), t);
-      t = fmaf(f.y - __ldg(vec + D + d + 1), __ldg(vec + d + 1), t);
+  for (int e = 0; e < E; ++e) vs[e] = ms[e] = 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int sr = __shfl_sync(0xffffffffu, slot, r);
+    acc[r] = 0.f;
+    if (sr >= 0) {  // the same for the whole warp
+      if (sr != cached) {
+        const float* vec = nodevec + (size_t)(bh * slots + sr) * 2 * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          vs[e] = __ldg(vec + e);
+          ms[e] = __ldg(vec + D + e);
+        }
+        cached = sr;
+      }
+      const __nv_bfloat162* x =
+          reinterpret_cast<const __nv_bfloat162*>(buf + r * D * 2 + lane * E * 2);
+      float t = 0.f;
+#pragma unroll
+      for (int h = 0; h < E / 2; ++h) {
+        const float2 f = __bfloat1622float2(x[h]);
+        t = fmaf(f.x - ms[2 * h], vs[2 * h], t);
+        t = fmaf(f.y - ms[2 * h + 1], vs[2 * h + 1], t);
+      }
+      acc[r] = t;
     }
   }
-  uint32_t u = __float_as_uint(t);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // unsigned order == float order
-  keys[(size_t)bh * N + p] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(token);
+  // transpose reduction: after the step of width w, a lane keeps the w rows
+  // whose index has its lane's bit w, summed with its partner's
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? acc[i] : acc[i + w];
+      const float keep = upper ? acc[i + w] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  if (slot >= 0) {
+    uint32_t u = __float_as_uint(acc[0]);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // unsigned order == float order
+    keys[(size_t)bh * N + p] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(token);
+  }
 }
 
 // ---------------------------------------------------------------- select + partition
@@ -552,26 +671,42 @@ __global__ void __launch_bounds__(kSplitThreads)
     }
     if (shift == 0) T = prefix;
   }
-  // stable partition by position: key <= T left, else right
-  uint32_t run_left = 0, run_right = 0;
-  for (int base = 0; base < nd.n; base += kSplitThreads) {
-    const int i = base + tid;
-    bool valid = i < nd.n, left = false;
-    if (valid) left = kk[i] <= T;
-    const uint32_t packed = valid ? (left ? (1u << 16) : 1u) : 0u;
-    uint32_t total;
-    const uint32_t incl = block_scan_incl(packed, wsum, &total);
-    const uint32_t excl = incl - packed;
+  // stable partition by position: key <= T left, else right.  Warp w owns
+  // the contiguous positions [w*len, (w+1)*len): it counts its left keys,
+  // the warps' counts are scanned, then each warp writes its range in order
+  // with ballots (no block barrier inside the loop).
+  constexpr int kWarps = kSplitThreads / 32;
+  const int lane = tid & 31, w = tid >> 5;
+  const int len = (nd.n + kWarps - 1) / kWarps;
+  const int lo = min(nd.n, w * len), hi = min(nd.n, lo + len);
+  uint32_t nleft = 0;
+  for (int b = lo; b < hi; b += 32) {
+    const int i = b + lane;
+    nleft += __popc(__ballot_sync(0xffffffffu, i < hi && kk[i] <= T));
+  }
+  __shared__ uint32_t wleft[kWarps];
+  if (lane == 0) wleft[w] = nleft;
+  __syncthreads();
+  uint32_t before_left = 0;
+  for (int v = 0; v < w; ++v) before_left += wleft[v];
+  uint32_t run_left = before_left, run_right = static_cast<uint32_t>(lo) - before_left;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b = lo; b < hi; b += 32) {
+    const int i = b + lane;
+    const bool valid = i < hi;
+    const bool left = valid && kk[i] <= T;
+    const unsigned ml = __ballot_sync(0xffffffffu, left);
+    const unsigned mr = __ballot_sync(0xffffffffu, valid && !left);
     if (valid) {
-      const int dst = left ? static_cast<int>(run_left + (excl >> 16))
-                           : nl + static_cast<int>(run_right + (excl & 0xFFFFu));
+      const int dst = left ? static_cast<int>(run_left + __popc(ml & lt))
+                           : nl + static_cast<int>(run_right + __popc(mr & lt));
       if (dst < nd.n && (left ? dst < nl : dst >= nl))
         out[dst] = in[i];
       else
         atomicOr(status, DEV_BOUNDS);
     }
-    run_left += total >> 16;
-    run_right += total & 0xFFFFu;
+    run_left += __popc(ml);
+    run_right += __popc(mr);
   }
 }
 
@@ -629,18 +764,22 @@ cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int layout, 
                            msmem);
   if (e != cudaSuccess) return e;
   const int psmem = 0;  // the power kernel's shared memory is static
+  e = cudaFuncSetAttribute(pddp_project_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           proj_smem_bytes<D>());
+  if (e != cudaSuccess) return e;
 
   for (int d = 0; d < depths; ++d) {
     const int slots = 1 << d;
     const int chunks = (max_node_rows(N, C, d) + kChunkRows - 1) / kChunkRows;
     pddp_moments_kernel<D><<<dim3(chunks, slots, BH), kMomThreads, msmem, stream>>>(
-        *tq, pa, N, C, d, slots, chunks, partials, status, layout, H, head0);
+        q, pa, N, C, d, slots, chunks, partials, status, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     pddp_power_kernel<D><<<dim3(slots, BH), kPowThreads, psmem, stream>>>(partials, N, C, d, slots,
                                                                           chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    pddp_project_kernel<D><<<dim3((N + 255) / 256, BH), 256, 0, stream>>>(
-        q, pa, N, C, d, slots, nodevec, keys, layout, H, head0);
+    pddp_project_kernel<D><<<dim3((N + kProjThreads - 1) / kProjThreads, BH), kProjThreads,
+                             proj_smem_bytes<D>(), stream>>>(q, pa, N, C, d, slots, nodevec, keys,
+                                                             layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
                                                                      status);
