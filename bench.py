@@ -547,12 +547,13 @@ SCHEDULES = [("small", 0.1, 3), ("small", 0.2, 3), ("small", 0.3, 3),
              ("long", 0.15, 2), ("long", 0.25, 2), ("asset3d", 0.15, 3)]
 
 
-def schedule_pass(p, steps, anchors, inputs, bufs, stream):
+def schedule_pass(p, steps, anchors, inputs, bufs, stream, pairs=None):
     """One pass over a denoising schedule: an anchor step (grouping, dense
     attention + LSE, exact selection, sparse attention recording the
     residual) at each anchor, a reuse step (sparse attention + cached
-    residual) otherwise, each on its own step's inputs.  Returns the events
-    bracketing every stage, in order."""
+    residual) otherwise, each on its own step's inputs.  With `pairs` (C = 64)
+    the anchor also builds the sibling-pair key lists and the sparse passes
+    run on them.  Returns the events bracketing every stage, in order."""
     from token_sparse_attention_gb300 import mcs
 
     perm, idx, dense, lse, res, out, retained, ws = bufs
@@ -572,9 +573,17 @@ def schedule_pass(p, steps, anchors, inputs, bufs, stream):
             mcs.mcs_dense_attn(p, q, k, v, dense, lse)
             mark("dense")
             mcs.mcs_select(p, q, k, lse, perm, idx, ws, retained)
+            if pairs is not None:
+                mcs.mcs_pair_lists(p, idx, pairs)
             mark("select")
-            mcs.mcs_sparse_attn_record(p, q, k, v, perm, idx, dense, res)
+            if pairs is not None:
+                mcs.mcs_sparse_attn_pairs_record(p, q, k, v, perm, pairs, dense, res)
+            else:
+                mcs.mcs_sparse_attn_record(p, q, k, v, perm, idx, dense, res)
             mark("record")
+        elif pairs is not None:
+            mcs.mcs_sparse_attn_pairs(p, q, k, v, perm, pairs, res, out)
+            mark("reuse")
         else:
             mcs.mcs_sparse_attn(p, q, k, v, perm, idx, res, out)
             mark("reuse")
@@ -610,11 +619,26 @@ def run_schedules(dev):
                 torch.empty_like(q0), torch.empty_like(q0),
                 torch.empty(w.B, w.H, G, dtype=torch.float32, device=dev),
                 mcs.empty_workspace(mcs.mcs_anchor_workspace(p), dev))
-        schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream)  # warm-up
+        # C = 64: sibling pairs share one 128-row tile over their key union
+        pairs = mcs.empty_pairs(p, dev) if mcs.mcs_pair_bytes(p) else None
+        schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream, pairs)  # warm-up
         torch.cuda.synchronize()
+        unpaired_ms = None
+        if pairs is not None:
+            # the same reuse launch without pairing, for comparison
+            q1, k1, v1 = inputs[1]
+            perm_, idx_, _, _, res_, out_ = bufs[:6]
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            mcs.mcs_sparse_attn(p, q1, k1, v1, perm_, idx_, res_, out_)
+            a_.record(stream)
+            for _ in range(3):
+                mcs.mcs_sparse_attn(p, q1, k1, v1, perm_, idx_, res_, out_)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            unpaired_ms = a_.elapsed_time(b_) / 3
         per = {}
         for _ in range(reps):
-            marks = schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream)
+            marks = schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream, pairs)
             torch.cuda.synchronize()
             for (_, a), (n, b) in zip(marks, marks[1:]):
                 per.setdefault(n, []).append(a.elapsed_time(b))
@@ -647,7 +671,12 @@ def run_schedules(dev):
             "passes": reps,
             "n_anchor": n_anchor, "n_reuse": n_reuse,
         }
-        del inputs, bufs, q0
+        if pairs is not None:
+            r = res_all[f"{name} s={density}"]
+            r["sibling_pairs"] = True
+            r["sparse_reuse_ms_unpaired"] = unpaired_ms
+            r["speedup_vs_dense_unpaired"] = stage["dense"] / unpaired_ms
+        del inputs, bufs, q0, pairs
         torch.cuda.empty_cache()
     return res_all
 

@@ -181,6 +181,39 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
                                   const void* dense_out, void* residual, cudaStream_t stream);
 
 /*
+ * Sibling-pair key lists for C = 64 groups: a kernel layout of idx, not a
+ * step of the method.  A C = 64 group fills half of the 128-row query tile of
+ * the tensor-core MMA, and a 64-row MMA takes as long as a 128-row one.
+ * Groups 2u and 2u+1 are siblings of the grouping tree (similar queries, so
+ * their index sets overlap heavily); mcs_sparse_attn_pairs runs them as one
+ * 128-row tile over the union of their index sets, adding -2^20 to the
+ * scores of keys a row's group did not select (through one more tensor-core
+ * step), so that every query still attends to exactly its own group's K
+ * tokens (wispaper.ai, "Token-level selection needs tile-aligned query
+ * groups"): results match mcs_sparse_attn up to summation order, on about
+ * |A u B| / 2K of the tensor work.
+ *
+ * mcs_pair_bytes: size of the pair-list buffer (0 when unsupported).
+ * mcs_pair_lists: idx [B,H,G,K] (rows ascending) -> pairs, a device buffer of
+ *   at least mcs_pair_bytes(p) bytes, 256-byte aligned (its layout is the
+ *   library's; build it once per anchor, like idx).  Requires C = 64,
+ *   K <= 16384, N < 2^28 (MCS_ERR_UNSUPPORTED otherwise); an index outside
+ *   [0, N) sets MCS_ERR_BOUNDS in the device status.
+ * mcs_sparse_attn_pairs / _pairs_record: as mcs_sparse_attn /
+ *   mcs_sparse_attn_record with the pair lists in place of idx.
+ */
+size_t mcs_pair_bytes(const mcs_params* p);
+mcs_status mcs_pair_lists(const mcs_params* p, const int32_t* idx, void* pairs,
+                          size_t pairs_bytes, cudaStream_t stream);
+mcs_status mcs_sparse_attn_pairs(const mcs_params* p, const void* q, const void* k,
+                                 const void* v, const int32_t* perm, const void* pairs,
+                                 const void* residual, void* out, cudaStream_t stream);
+mcs_status mcs_sparse_attn_pairs_record(const mcs_params* p, const void* q, const void* k,
+                                        const void* v, const int32_t* perm, const void* pairs,
+                                        const void* dense_out, void* residual,
+                                        cudaStream_t stream);
+
+/*
  * The whole anchor step (wispaper.ai, "Reused exact selection beats
  * recomputed mean pooling"; "Residual correction recovers the discarded
  * tail"): a1 grouping -> perm; a2 dense attention -> dense_out (the step's

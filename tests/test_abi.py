@@ -142,3 +142,24 @@ def test_layout_field_is_checked_on_the_host(L):
         assert L.mcs_dense_attn(ctypes.byref(p), 16, 16, 16, 16, None, None) == want
         assert L.mcs_meta_bytes(ctypes.byref(p)) == 0
     assert ctypes.sizeof(mcs.Params) == 9 * 4
+
+
+def test_pair_lists_host_checks(L):
+    # sibling-pair lists: C = 64 only, K up to 16384; buffer of P = ceil(G/2)
+    # lengths, then P rows of the union capacity (2K rounded up to 128)
+    p = mcs.params(1, 2, 1000, 128, 64, 300)  # G = 16, P = 8
+    n = mcs.mcs_pair_bytes(p)
+    cap = -(-2 * 300 // 128) * 128
+    off = -(-2 * 8 * 4 // 256) * 256
+    assert n == off + 2 * 8 * cap * 4
+    assert mcs.mcs_pair_bytes(mcs.params(1, 2, 1000, 128, 128, 300)) == 0  # C = 128
+    assert mcs.mcs_pair_bytes(mcs.params(1, 1, 40000, 128, 64, 16385)) == 0  # K too large
+    q = mcs.params(1, 2, 1000, 128, 128, 300)
+    assert L.mcs_pair_lists(ctypes.byref(q), 256, 256, 1 << 20, None) == 2
+    assert L.mcs_sparse_attn_pairs(ctypes.byref(q), 16, 16, 16, 16, 256, None, 16, None) == 2
+    assert L.mcs_pair_lists(ctypes.byref(p), None, 256, n, None) == 1  # null idx
+    assert L.mcs_pair_lists(ctypes.byref(p), 256, 16, n, None) == 1  # pairs not 256-aligned
+    assert L.mcs_pair_lists(ctypes.byref(p), 256, 256, n - 4, None) == 3  # too small
+    assert L.mcs_sparse_attn_pairs(ctypes.byref(p), 16, 16, 16, 16, None, None, 16, None) == 1
+    assert L.mcs_sparse_attn_pairs_record(ctypes.byref(p), 16, 16, 16, 16, 256, None, 16,
+                                          None) == 1  # record needs dense_out

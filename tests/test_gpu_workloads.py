@@ -149,6 +149,19 @@ def test_workload_full_size(name, density):
         want = orc.sparse_attention_group(qh, kh, vh, m, oidx[g], scale) + P.f64(r0)[m]
         P.assert_close(out0[torch.from_numpy(m).cuda()], want, f"{name} sparse g{g}")
     assert mcs.mcs_device_status() == 0
+    if mcs.mcs_pair_bytes(p):
+        # C = 64: the sibling-pair path on the same groups and index sets
+        pairs = mcs.empty_pairs(p)
+        mcs.mcs_pair_lists(p, idx_in, pairs)
+        outp = torch.empty_like(q)
+        mcs.mcs_sparse_attn_pairs(p, q, k, v, perm_in, pairs, res_in, outp)
+        outp0 = outp.view(BH, w.N, w.D)[0]
+        for g in groups:
+            m = members[g]
+            want = orc.sparse_attention_group(qh, kh, vh, m, oidx[g], scale) + P.f64(r0)[m]
+            P.assert_close(outp0[torch.from_numpy(m).cuda()], want, f"{name} pairs g{g}")
+        assert mcs.mcs_device_status() == 0
+        del pairs, outp
 
     # ---- grouping of head 0 against the oracle's (fp32 vs fp64 projections
     # may move near-median tokens)

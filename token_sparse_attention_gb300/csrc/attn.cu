@@ -60,15 +60,21 @@ constexpr float kRescaleThreshold = 16.0f;
 // (sparse, 4 items per step).  16 covers both rings (NS <= 12).
 constexpr int kDone = 16;
 
-template <int D>
+template <int D, bool PAIRS>
 struct AttnLayout {
   static constexpr int kSub = D / 64;          // 128-byte column sub-tiles per row
   static constexpr int kSubBytes = 128 * 128;  // one sub-tile: 128 rows x 128 B
   static constexpr int kTileBytes = kSub * kSubBytes;  // a 128-row tile of Q, K or V
-  static constexpr int kStages = D == 128 ? 5 : 12;    // K/V ring depth (tiles)
+  // paired mode: each stage also holds the mask operand of a K tile (128 keys
+  // x 16 bf16, K-major without swizzle), and one more 128 x 16 operand holds
+  // the rows' group selectors
+  static constexpr int kMaskBytes = PAIRS ? 128 * 32 : 0;
+  static constexpr int kStageBytes = kTileBytes + kMaskBytes;
+  static constexpr int kStages = PAIRS ? (D == 128 ? 4 : 9) : (D == 128 ? 5 : 12);  // ring depth
   static constexpr int kQ = 0;                         // Q_a, Q_b
-  static constexpr int kRing = 2 * kTileBytes;
-  static constexpr int kBars = kRing + kStages * kTileBytes;
+  static constexpr int kRowSel = 2 * kTileBytes;       // paired mode: row group selectors
+  static constexpr int kRing = kRowSel + kMaskBytes;
+  static constexpr int kBars = kRing + kStages * kStageBytes;
   static constexpr int kNumBars = kStages + kDone + 3;
   static constexpr int kSmem = kBars + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -113,6 +119,17 @@ __device__ __forceinline__ float max64(const float* s) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
+// Paired mode: the 16-byte K-major chunk (elements 0-7 of the mask step's K
+// dimension) of row r of a 128 x 16 bf16 operand without swizzle, stored as
+// 8-row x 16-byte core matrices (the two K halves of an 8-row group adjacent).
+__device__ __forceinline__ int mask_row_offset(int r) { return (r >> 3) * 256 + (r & 7) * 16; }
+
+// Mask chunk of a key by its group membership bits (bit 0: in the pair's
+// first group, bit 1: in its second): elements (k0, k1) = 0 for the groups
+// that selected the key and -2^20 for the others; bf16 -2^20 = 0xC980.
+__device__ __align__(16) uint4 g_pair_mask[4] = {
+    {0xC980C980u, 0u, 0u, 0u}, {0xC9800000u, 0u, 0u, 0u}, {0x0000C980u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+
 // Byte offset of 16-byte chunk `seg` of row r in a 128-row tile stored as
 // 128-byte-swizzled K-major sub-tiles (the layout TMA writes with SW128).
 __device__ __forceinline__ int swz_offset(int r, int seg) {
@@ -123,7 +140,9 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
-  using L = AttnLayout<D>;
+  constexpr bool kPairs = (MODE & kPaired) != 0;
+  constexpr int kBase = MODE & 3;  // kDense, kSparse, kSparseAdd or kSparseRecord
+  using L = AttnLayout<D, kPairs>;
   constexpr int NS = L::kStages;
   constexpr bool kSparseMode = MODE != kDense;
   extern __shared__ uint8_t smem_raw[];
@@ -145,10 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.y;
   const int head_h = bh % a.H, head_b = bh / a.H;    // tile-map coordinates of this head
   const RowMap rm = row_map(a.layout, a.H, a.N, bh);  // rows of q/k/v/out in either layout
-  const int units = kSparseMode ? a.G : (a.N + BM - 1) / BM;  // units per head
+  // units per head: query tiles (dense), groups (sparse) or sibling pairs of
+  // C = 64 groups (paired)
+  const int units = kSparseMode ? (kPairs ? a.P : a.G) : (a.N + BM - 1) / BM;
   const bool has_b = 2 * pair + 1 < units;
   const int kv_total = kSparseMode ? a.K : a.N;
-  const int nkv = (kv_total + BN - 1) / BN;
+  // keys per unit: a pair's union list is as long as its plen entry
+  int kv_len[2] = {kv_total, kv_total};
+  if (kPairs) {
+    kv_len[0] = __ldg(a.plen + static_cast<size_t>(bh) * a.P + 2 * pair);
+    kv_len[1] = has_b ? __ldg(a.plen + static_cast<size_t>(bh) * a.P + 2 * pair + 1) : kv_len[0];
+    kv_len[0] = min(max(kv_len[0], 1), a.cap);
+    kv_len[1] = min(max(kv_len[1], 1), a.cap);
+  }
+  const int nkv = (max(kv_len[0], kv_len[1]) + BN - 1) / BN;
   // Ring items, numbered in the order the MMA warp consumes them (item i
   // goes to stage i % NS).  Dense: K(j) = 2j, V(j) = 2j+1, each shared by
   // both units.  Sparse: K_a(0) = 0, K_b(0) = 1, then per step j
@@ -185,6 +214,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  if constexpr (kPairs) {
+    // row selectors: rows 0-63 (the pair's first group) take mask element
+    // k0, rows 64-127 element k1 (bf16 1.0 = 0x3F80); the stages' mask
+    // operands start zeroed (their second K half stays zero)
+    uint8_t* rsel = smem + L::kRowSel;
+    for (int r = threadIdx.x; r < 128; r += kThreads) {
+      *reinterpret_cast<uint4*>(rsel + mask_row_offset(r)) =
+          make_uint4(r < 64 ? 0x3F80u : 0x3F800000u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(rsel + mask_row_offset(r) + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = threadIdx.x; i < NS * (L::kMaskBytes / 16); i += kThreads) {
+      const int st = i / (L::kMaskBytes / 16), o = i % (L::kMaskBytes / 16);
+      reinterpret_cast<uint4*>(smem + L::kRing + st * L::kStageBytes + L::kTileBytes)[o] =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -214,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elect_one()) {
             mbar_expect_tx(full + st, L::kTileBytes);
             const CUtensorMap* tm = (i & 1) ? &tv : &tk;
-            uint8_t* dst = ring + st * L::kTileBytes;
+            uint8_t* dst = ring + st * L::kStageBytes;
             for (int s = 0; s < L::kSub; ++s)
               tma_load_4d(dst + s * L::kSubBytes, tm, s * 64, (i >> 1) * BN, head_h, head_b,
                           full + st);
@@ -247,16 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sub = lane / kSegs, seg = lane % kSegs;
       const int group[2] = {2 * pair, has_b ? 2 * pair + 1 : 2 * pair};
       bool bad = false;
-      // Q rows of both units (perm order); padding slots, rows >= C and a
-      // missing unit b are zero rows.
+      // Q rows of both units (perm order); padding slots, rows past the
+      // unit's queries and a missing unit b are zero rows.  A pair's rows are
+      // the perm rows of its two groups, which are adjacent in perm.
       for (int x = 0; x < 2; ++x) {
-        const int32_t* perm_g = a.perm + (static_cast<size_t>(bh) * a.G + group[x]) * a.C;
+        const int32_t* perm_g =
+            a.perm + (static_cast<size_t>(bh) * a.G + (kPairs ? 2 * group[x] : group[x])) * a.C;
+        const int qrows = kPairs ? (2 * group[x] + 1 < a.G ? 2 : 1) * a.C : a.C;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int c = tid + kPT * k;
           if (c < kChunks) {
             const int r = c / kSegs, sg = c % kSegs;
-            int tok = (r < a.C && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
+            int tok = (r < qrows && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
             if (tok >= a.N) { bad = true; tok = -1; }
             const __nv_bfloat16* src =
                 a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + sg * 8;
@@ -269,24 +318,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       // holds the row of group pw + kProducers * (l / kRPI), sub-row l % kRPI.
       // Loaded two tiles ahead so that the index latency (the index array is
       // read once, from HBM) stays off the critical path.
-      auto load_rows = [&](int x, int j) -> int {
-        const int32_t* idx_g = a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K;
+      // Paired mode: the pair's union list instead (no tail clamp: lists are
+      // padded to whole tiles); the entry's group bits go to *bits.
+      auto load_rows = [&](int x, int j, int* bits) -> int {
+        const int32_t* idx_g =
+            kPairs ? a.pidx + (static_cast<size_t>(bh) * a.P + group[x]) * a.cap
+                   : a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K;
         int out = 0;
+        *bits = 0;
         if (lane < kGPW * kRPI) {
           const int rg = pw + kProducers * (lane / kRPI);
           int col = j * BN + (rg < kRG ? rg * kRPI + lane % kRPI : 0);
-          col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked in softmax
+          if (!kPairs) col = col < a.K ? col : a.K - 1;  // tail rows repeat a valid row; masked
           int tok = __ldg(idx_g + col);
+          if (kPairs) {
+            *bits = static_cast<int>((static_cast<uint32_t>(tok) >> kPairTokenBits) & 3u);
+            tok &= (1 << kPairTokenBits) - 1;
+          }
           if (tok < 0 || tok >= a.N) { bad = true; tok = 0; }
           out = rm.rbase + tok * rm.rstride;
         }
         return out;
       };
-      // Copy the rows of one K or V tile into the stage of ring item `it`.
-      auto copy_tile = [&](int it, const __nv_bfloat16* src, int rows) -> bool {
+      // Copy the rows of one K or V tile into the stage of ring item `it`;
+      // paired mode, K tiles: also each key's mask chunk (by its group bits)
+      // into the stage's mask operand.
+      auto copy_tile = [&](int it, const __nv_bfloat16* src, int rows, int bits,
+                           bool is_k) -> bool {
         const int st = it % NS;
         if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
-        uint8_t* stage = ring + st * L::kTileBytes;
+        uint8_t* stage = ring + st * L::kStageBytes;
 #pragma unroll
         for (int i = 0; i < kGPW; ++i) {
           const int rg = pw + kProducers * i;
@@ -294,43 +355,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rg < kRG)
             cp_async16(stage + swz_offset(rg * kRPI + sub, seg),
                        src + static_cast<size_t>(row) * D + seg * 8);
+          if (kPairs && is_k) {
+            const int b = __shfl_sync(0xffffffffu, bits, i * kRPI + sub);
+            if (rg < kRG && seg == 0)
+              cp_async16(stage + L::kTileBytes + mask_row_offset(rg * kRPI + sub), g_pair_mask + b);
+          }
         }
         cp_async_arrive(full + st);
         ++issued;
         return true;
       };
-      // Both groups' index rows (K entries each) are read once, from HBM:
-      // pull them into L2 now so that the per-tile index loads below hit L2.
+      // Both units' index rows are read once, from HBM: pull them into L2
+      // now so that the per-tile index loads below hit L2.
       for (int x = 0; x < 2; ++x) {
         const char* idx_g = reinterpret_cast<const char*>(
-            a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K);
-        for (int off = tid * 128; off < a.K * 4; off += kPT * 128)
+            kPairs ? a.pidx + (static_cast<size_t>(bh) * a.P + group[x]) * a.cap
+                   : a.idx + (static_cast<size_t>(bh) * a.G + group[x]) * a.K);
+        const int bytes = (kPairs ? kv_len[x] : a.K) * 4;
+        for (int off = tid * 128; off < bytes; off += kPT * 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(idx_g + off));
       }
-      // rows of tiles j (V_x(j)), j+1 (K_x(j+1)) and j+2 (being fetched)
+      // rows (and paired-mode group bits) of tiles j (V_x(j)), j+1 (K_x(j+1))
+      // and j+2 (being fetched)
       int r0[2], r1[2] = {0, 0}, r2[2] = {0, 0};
-      r0[0] = load_rows(0, 0);
-      r0[1] = load_rows(1, 0);
+      int b0[2], b1[2] = {0, 0}, b2[2] = {0, 0};
+      r0[0] = load_rows(0, 0, &b0[0]);
+      r0[1] = load_rows(1, 0, &b0[1]);
       if (nkv > 1) {
-        r1[0] = load_rows(0, 1);
-        r1[1] = load_rows(1, 1);
+        r1[0] = load_rows(0, 1, &b1[0]);
+        r1[1] = load_rows(1, 1, &b1[1]);
       }
-      bool ok = copy_tile(k_item(0, 0), a.k, r0[0]) && copy_tile(k_item(1, 0), a.k, r0[1]);
+      bool ok = copy_tile(k_item(0, 0), a.k, r0[0], b0[0], true) &&
+                copy_tile(k_item(1, 0), a.k, r0[1], b0[1], true);
       for (int j = 0; ok && j < nkv; ++j) {
         if (a.fault && j >= 1) break;  // test-only: starve the MMA warp
         const bool more = j + 1 < nkv;
         for (int x = 0; ok && x < 2; ++x)
-          ok = copy_tile(v_item(x, j), a.v, r0[x]) && (!more || copy_tile(k_item(x, j + 1), a.k, r1[x]));
+          ok = copy_tile(v_item(x, j), a.v, r0[x], 0, false) &&
+               (!more || copy_tile(k_item(x, j + 1), a.k, r1[x], b1[x], true));
         // indices of tile j+2, after this step's copies: their load latency
         // then delays nothing already due
         if (j + 2 < nkv) {
-          r2[0] = load_rows(0, j + 2);
-          r2[1] = load_rows(1, j + 2);
+          r2[0] = load_rows(0, j + 2, &b2[0]);
+          r2[1] = load_rows(1, j + 2, &b2[1]);
         }
         r0[0] = r1[0];
         r0[1] = r1[1];
         r1[0] = r2[0];
         r1[1] = r2[1];
+        b0[0] = b1[0];
+        b0[1] = b1[1];
+        b1[0] = b2[0];
+        b1[1] = b2[1];
       }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
       if (*abort_flag) asm volatile("cp.async.wait_all;" ::: "memory");  // copies land first
@@ -351,11 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
     const uint32_t ring_addr = smem_u32(ring);
     const uint32_t q_addr = smem_u32(qs);
-    auto stage_addr = [&](int item) { return ring_addr + (item % NS) * L::kTileBytes; };
+    auto stage_addr = [&](int item) { return ring_addr + (item % NS) * L::kStageBytes; };
     auto wait_item = [&](int item) {
       return warp_wait(full + item % NS, (item / NS) & 1, abort_flag, a.status);
     };
-    // S_x(j) = Q_x K(j)^T (issuing lane only)
+    // S_x(j) = Q_x K(j)^T (issuing lane only); paired mode: plus one K = 16
+    // step of row selectors x key masks, which adds -2^20 to the scores of
+    // keys the row's group did not select (exactly 0 to the others)
     auto issue_qk = [&](int x, int j) {
       const int i = k_item(x, j);
       const uint32_t kb = stage_addr(i), qb = q_addr + x * L::kTileBytes;
@@ -365,6 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_ss(tmem + x * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                 idesc_qk, kk > 0);
       }
+      if (kPairs)
+        umma_ss(tmem + x * 128, sdesc_none(smem_u32(smem + L::kRowSel), 128, 256),
+                sdesc_none(kb + L::kTileBytes, 128, 256), idesc_qk, 1u);
     };
     // O_x (+)= P_x(j) V(j), A = P from TMEM (issuing lane only)
     auto issue_pv = [&](int x, int j) {
@@ -422,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 64-127 over columns 32-63, read in the first half.
     const int x = warp >> 2;
     const int row = (warp & 3) * 32 + lane;  // 0..127 == TMEM lane
+    const int kv_mine = x == 0 ? kv_len[0] : kv_len[1];  // keys of this warp's unit
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + x * 128 + lane_off;
     const uint32_t tO = tmem + 256 + x * D + lane_off;
@@ -434,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int valid = kv_total - j * BN;
+      const int valid = kv_mine - j * BN;
       float s[64];
       uint32_t* su = reinterpret_cast<uint32_t*>(s);
       tmem_ld32(tS + 64, su);
@@ -528,8 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         token = unit * BM + row;
         if (token >= a.N) token = -1;
       } else {
-        token = (row < a.C && (x == 0 || has_b))
-                    ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + unit) * a.C + row)
+        // a pair's 2C rows are the perm rows of its two groups (the second
+        // may not exist when G is odd)
+        const int g0 = kPairs ? 2 * unit : unit;
+        const int qrows = kPairs ? (g0 + 1 < a.G ? 2 : 1) * a.C : a.C;
+        token = (row < qrows && (x == 0 || has_b))
+                    ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g0) * a.C + row)
                     : -1;
         if (token >= a.N) token = -1;
       }
@@ -544,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv_l;
-          if (MODE == kSparseAdd || MODE == kSparseRecord) {
+          if (kBase == kSparseAdd || kBase == kSparseRecord) {
             const uint4* src = reinterpret_cast<const uint4*>(a.aux_in + row_off + c * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -554,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 float2 f2 = __bfloat1622float2(hh[e]);
                 const int i0 = q4 * 8 + 2 * e;
-                if (MODE == kSparseAdd) {
+                if (kBase == kSparseAdd) {
                   v[i0] += f2.x;
                   v[i0 + 1] += f2.y;
                 } else {
@@ -592,10 +678,11 @@ template <int D, int MODE>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const AttnArgs& a, int BH, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, MODE>;
-  const int smem = AttnLayout<D>::kSmem;
+  constexpr bool kPairs = (MODE & kPaired) != 0;
+  const int smem = AttnLayout<D, kPairs>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int units = (MODE == kDense) ? (a.N + BM - 1) / BM : a.G;
+  const int units = (MODE == kDense) ? (a.N + BM - 1) / BM : (kPairs ? a.P : a.G);
   kern<<<dim3((units + 1) / 2, BH), kThreads, smem, stream>>>(*tq, *tk, *tv, a);
   return cudaGetLastError();
 }
@@ -606,7 +693,7 @@ cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUten
                              const CUtensorMap* tv, const AttnArgs& a, int BH,
                              cudaStream_t stream) {
 #define MCS_ATTN_CASE(DD, MM) \
-  if (D == DD && mode == MM) return launch_one<DD, MM>(tq, tk, tv, a, BH, stream);
+  if (D == (DD) && mode == (MM)) return launch_one<DD, MM>(tq, tk, tv, a, BH, stream);
   MCS_ATTN_CASE(128, kDense)
   MCS_ATTN_CASE(128, kSparse)
   MCS_ATTN_CASE(128, kSparseAdd)
@@ -615,6 +702,12 @@ cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUten
   MCS_ATTN_CASE(64, kSparse)
   MCS_ATTN_CASE(64, kSparseAdd)
   MCS_ATTN_CASE(64, kSparseRecord)
+  MCS_ATTN_CASE(128, kSparse | kPaired)
+  MCS_ATTN_CASE(128, kSparseAdd | kPaired)
+  MCS_ATTN_CASE(128, kSparseRecord | kPaired)
+  MCS_ATTN_CASE(64, kSparse | kPaired)
+  MCS_ATTN_CASE(64, kSparseAdd | kPaired)
+  MCS_ATTN_CASE(64, kSparseRecord | kPaired)
 #undef MCS_ATTN_CASE
   return cudaErrorInvalidValue;
 }

@@ -47,7 +47,30 @@ enum AttnMode : int {
   kSparse = 1,        // token-sparse attention, writes O' scattered to perm rows
   kSparseAdd = 2,     // token-sparse attention + cached residual (reuse step)
   kSparseRecord = 3,  // token-sparse attention, writes residual = dense_out - O' (anchor)
+  kPaired = 4,        // flag on a sparse mode: C = 64 sibling pairs over their key unions
 };
+
+// Sibling-pair key lists (C = 64): groups 2u and 2u+1 of a head form pair u
+// (P = ceil(G/2) pairs; the last pair has one group when G is odd).  Each
+// pair's list is the ascending union of the two groups' index sets, entry =
+// token | (in group 2u) << 28 | (in group 2u+1) << 29, padded to `cap`
+// entries (token 0, in neither group).  Buffer: lens [BH*P] int32, then
+// entries [BH*P, cap] int32 at a 256-byte aligned offset.
+struct PairLayout {
+  int P, cap;
+  size_t entries_off, total;
+};
+__host__ __device__ inline PairLayout pair_layout(int BH, int G, int K) {
+  PairLayout l;
+  l.P = (G + 1) / 2;
+  l.cap = (2 * K + 127) / 128 * 128;
+  l.entries_off = ((size_t)BH * l.P * 4 + 255) / 256 * 256;
+  l.total = l.entries_off + (size_t)BH * l.P * l.cap * 4;
+  return l;
+}
+constexpr int kPairMaxK = 16384;           // the union kernel keeps 3K + 1 ints in shared memory
+constexpr int kPairTokenBits = 28;         // tokens below 2^28
+constexpr float kPairMaskBias = -1048576.f;  // -2^20: added to the scores of other groups' keys
 
 struct AttnArgs {
   int H, layout;     // heads per batch entry; tensor layout (see RowMap)
@@ -66,6 +89,10 @@ struct AttnArgs {
   const __nv_bfloat16* v;        // [BH, N, D]
   unsigned* status;              // device status word
   int fault;                     // test-only: 1 = producers stop after the first K/V tile
+  // kPaired: pair lists (see PairLayout)
+  int P, cap;
+  const int32_t* plen;           // [BH, P]
+  const int32_t* pidx;           // [BH, P, cap]
 };
 
 // tq/tk/tv: dense -> 4-D tile maps [B][H][N][D] in the tensors' layout, box
@@ -102,6 +129,10 @@ cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* t
 // kernel; with it most rows are selected in one read of their masses.
 cudaError_t launch_topk(const float* mass, const uint32_t* hist, int rows, int n, int K,
                         int32_t* idx, float* retained, unsigned* status, cudaStream_t stream);
+
+// idx [BH, G, K] (rows ascending) -> pair lists in `pairs` (PairLayout).
+cudaError_t launch_pair_union(const int32_t* idx, int BH, int G, int K, int N, void* pairs,
+                              unsigned* status, cudaStream_t stream);
 
 // Device address of the library's status word (for kernels' status argument).
 cudaError_t device_status_word(unsigned** out);

@@ -118,12 +118,24 @@ int fault_from_env() {
   return (f != nullptr && strcmp(f, "stall_load") == 0) ? 1 : 0;
 }
 
-mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const void* v,
-                      const int32_t* perm, const int32_t* idx, const void* aux, void* out,
-                      int mode, cudaStream_t stream) {
+// Paired-mode requirements (pair lists, see PairLayout): C = 64, K small
+// enough for the union kernel's shared memory, tokens below 2^28.
+mcs_status check_pairs(const mcs_params* p) {
   mcs_status s = check_shape(p, true);
   if (s != MCS_OK) return s;
-  if (!q || !k || !v || !perm || !idx || !out) return MCS_ERR_INVALID_ARG;
+  if (p->C != 64 || p->K > mcs::kPairMaxK || p->N >= (1 << mcs::kPairTokenBits))
+    return MCS_ERR_UNSUPPORTED;
+  return MCS_OK;
+}
+
+mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const void* v,
+                      const int32_t* perm, const int32_t* idx, const void* aux, void* out,
+                      int mode, cudaStream_t stream, const void* pairs = nullptr) {
+  mcs_status s = check_shape(p, true);
+  if (s != MCS_OK) return s;
+  if (pairs && (s = check_pairs(p)) != MCS_OK) return s;
+  if (!q || !k || !v || !perm || (!idx && !pairs) || !out) return MCS_ERR_INVALID_ARG;
+  if (pairs && (reinterpret_cast<uintptr_t>(pairs) & 255u) != 0) return MCS_ERR_INVALID_ARG;
   if (mode != mcs::kSparse && !aux) return MCS_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (aux && !aligned16(aux)))
@@ -150,6 +162,14 @@ mcs_status run_sparse(const mcs_params* p, const void* q, const void* k, const v
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
   a.fault = fault_from_env();
+  if (pairs) {
+    const mcs::PairLayout l = mcs::pair_layout(BH, a.G, p->K);
+    a.P = l.P;
+    a.cap = l.cap;
+    a.plen = static_cast<const int32_t*>(pairs);
+    a.pidx = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(pairs) + l.entries_off);
+    mode |= mcs::kPaired;
+  }
   if ((s = status_ptr(&a.status)) != MCS_OK) return s;
   cudaError_t e = mcs::launch_attention(p->D, mode, &tq, &tk, &tv, a, BH, stream);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
@@ -351,6 +371,43 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
                                   const void* v, const int32_t* perm, const int32_t* idx,
                                   const void* dense_out, void* residual, cudaStream_t stream) {
   return run_sparse(p, q, k, v, perm, idx, dense_out, residual, mcs::kSparseRecord, stream);
+}
+
+size_t mcs_pair_bytes(const mcs_params* p) {
+  if (check_pairs(p) != MCS_OK) return 0;
+  return mcs::pair_layout(p->B * p->H, groups_of(p), p->K).total;
+}
+
+mcs_status mcs_pair_lists(const mcs_params* p, const int32_t* idx, void* pairs,
+                          size_t pairs_bytes, cudaStream_t stream) {
+  mcs_status s = check_pairs(p);
+  if (s != MCS_OK) return s;
+  if (!idx || !pairs) return MCS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pairs) & 255u) != 0) return MCS_ERR_INVALID_ARG;
+  if (pairs_bytes < mcs_pair_bytes(p)) return MCS_ERR_WORKSPACE;
+  unsigned* st;
+  if ((s = status_ptr(&st)) != MCS_OK) return s;
+  cudaError_t e =
+      mcs::launch_pair_union(idx, p->B * p->H, groups_of(p), p->K, p->N, pairs, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pair lists launch");
+  return MCS_OK;
+}
+
+mcs_status mcs_sparse_attn_pairs(const mcs_params* p, const void* q, const void* k,
+                                 const void* v, const int32_t* perm, const void* pairs,
+                                 const void* residual, void* out, cudaStream_t stream) {
+  if (!pairs) return MCS_ERR_INVALID_ARG;
+  return run_sparse(p, q, k, v, perm, nullptr, residual, out,
+                    residual ? mcs::kSparseAdd : mcs::kSparse, stream, pairs);
+}
+
+mcs_status mcs_sparse_attn_pairs_record(const mcs_params* p, const void* q, const void* k,
+                                        const void* v, const int32_t* perm, const void* pairs,
+                                        const void* dense_out, void* residual,
+                                        cudaStream_t stream) {
+  if (!pairs) return MCS_ERR_INVALID_ARG;
+  return run_sparse(p, q, k, v, perm, nullptr, dense_out, residual, mcs::kSparseRecord, stream,
+                    pairs);
 }
 
 mcs_status mcs_select(const mcs_params* p, const void* q, const void* k, const float* lse,

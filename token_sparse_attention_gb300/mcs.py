@@ -23,7 +23,8 @@ __all__ = [
     "mcs_group_mass", "mcs_topk", "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record",
     "mcs_anchor_select", "mcs_group_noalloc", "mcs_meta_bytes", "mcs_meta_offsets",
     "meta_views", "mcs_meta_pack", "mcs_meta_unpack", "Stager", "mcs_block_workspace", "mcs_block_topk", "mcs_pooled_block_select",
-    "mcs_gather_mass", "mcs_rel_l1",
+    "mcs_gather_mass", "mcs_rel_l1", "mcs_pair_bytes", "empty_pairs", "mcs_pair_lists",
+    "mcs_sparse_attn_pairs", "mcs_sparse_attn_pairs_record",
 ]
 
 # Every symbol include/mcs.h declares.
@@ -31,6 +32,7 @@ EXPORTED = (
     "mcs_status_string", "mcs_last_cuda_error", "mcs_device_status", "mcs_group_workspace",
     "mcs_anchor_workspace", "mcs_group", "mcs_dense_attn", "mcs_group_mass", "mcs_topk",
     "mcs_select", "mcs_sparse_attn", "mcs_sparse_attn_record", "mcs_anchor_select", "mcs_group_noalloc",
+    "mcs_pair_bytes", "mcs_pair_lists", "mcs_sparse_attn_pairs", "mcs_sparse_attn_pairs_record",
     "mcs_meta_bytes", "mcs_meta_offsets", "mcs_meta_pack", "mcs_meta_unpack",
     "mcs_stager_create", "mcs_stager_destroy",
     "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait", "mcs_block_workspace",
@@ -90,6 +92,10 @@ _SIGS = {
     "mcs_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
     "mcs_sparse_attn": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_sparse_attn_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
+    "mcs_pair_bytes": ([_pp], _sz),
+    "mcs_pair_lists": ([_pp, _vp, _vp, _sz, _vp], _st),
+    "mcs_sparse_attn_pairs": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
+    "mcs_sparse_attn_pairs_record": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _st),
     "mcs_anchor_select": ([_pp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _st),
     "mcs_group_noalloc": ([_pp, _vp, _vp, _vp], _st),
     "mcs_meta_bytes": ([_pp], _sz),
@@ -245,6 +251,47 @@ def mcs_sparse_attn_record(p: Params, q, k, v, perm, idx, dense_out, residual, s
         _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
         _ptr(dense_out, bf, s, "dense_out"), _ptr(residual, bf, s, "residual"),
         _stream(stream)), "mcs_sparse_attn_record")
+
+
+def mcs_pair_bytes(p: Params) -> int:
+    """Bytes of the sibling-pair key-list buffer (0: unsupported for p)."""
+    return lib().mcs_pair_bytes(ctypes.byref(p))
+
+
+def empty_pairs(p: Params, device="cuda"):
+    """A device buffer for mcs_pair_lists (uint8, 256-byte aligned)."""
+    n = mcs_pair_bytes(p)
+    if n == 0:
+        raise ValueError("pair lists need C = 64, K <= 16384 and N < 2^28")
+    return empty_workspace(n, device)
+
+
+def mcs_pair_lists(p: Params, idx, pairs, stream=None):
+    _check(lib().mcs_pair_lists(
+        ctypes.byref(p), _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(pairs, torch.uint8, None, "pairs"), pairs.numel(), _stream(stream)),
+        "mcs_pair_lists")
+
+
+def mcs_sparse_attn_pairs(p: Params, q, k, v, perm, pairs, residual, out, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_sparse_attn_pairs(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"), _ptr(v, bf, s, "v"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(pairs, torch.uint8, None, "pairs"),
+        _ptr(residual, bf, s, "residual", optional=True), _ptr(out, bf, s, "out"),
+        _stream(stream)), "mcs_sparse_attn_pairs")
+
+
+def mcs_sparse_attn_pairs_record(p: Params, q, k, v, perm, pairs, dense_out, residual,
+                                 stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    _check(lib().mcs_sparse_attn_pairs_record(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _ptr(k, bf, s, "k"), _ptr(v, bf, s, "v"),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(pairs, torch.uint8, None, "pairs"),
+        _ptr(dense_out, bf, s, "dense_out"), _ptr(residual, bf, s, "residual"),
+        _stream(stream)), "mcs_sparse_attn_pairs_record")
 
 
 def mcs_select(p: Params, q, k, lse, perm, idx, ws, retained=None, stream=None):
