@@ -619,8 +619,12 @@ def run_schedules(dev):
                 torch.empty_like(q0), torch.empty_like(q0),
                 torch.empty(w.B, w.H, G, dtype=torch.float32, device=dev),
                 mcs.empty_workspace(mcs.mcs_anchor_workspace(p), dev))
-        # C = 64: sibling pairs share one 128-row tile over their key union
-        pairs = mcs.empty_pairs(p, dev) if mcs.mcs_pair_bytes(p) else None
+        # C = 64: sibling pairs share one 128-row tile over their key union,
+        # when the paired grid (two pairs per CTA) still fills the GPU twice
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        paired_ctas = w.B * w.H * (-(-G // 2)) / 2
+        pairs = (mcs.empty_pairs(p, dev)
+                 if mcs.mcs_pair_bytes(p) and paired_ctas >= 2 * sms else None)
         schedule_pass(p, w.steps, w.anchors, inputs, bufs, stream, pairs)  # warm-up
         torch.cuda.synchronize()
         unpaired_ms = None

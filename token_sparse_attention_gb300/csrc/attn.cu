@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kPairs && is_k) {
             const int b = __shfl_sync(0xffffffffu, bits, i * kRPI + sub);
             if (rg < kRG && seg == 0)
-              cp_async16(stage + L::kTileBytes + mask_row_offset(rg * kRPI + sub), g_pair_mask + b);
+              cp_async16_ca(stage + L::kTileBytes + mask_row_offset(rg * kRPI + sub), g_pair_mask + b);
           }
         }
         cp_async_arrive(full + st);

@@ -132,6 +132,13 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 
+// 16-byte global -> shared copy cached in L1 (for small tables every thread
+// of the SM reads: from L2 alone, one hot line serialises them), asynchronous.
+__device__ __forceinline__ void cp_async16_ca(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
 // As cp_async16, but when !valid nothing is read and the 16 bytes are zeroed
 // (src must still be a mapped address).
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
