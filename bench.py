@@ -49,10 +49,12 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # sha1 of the kernel source it was measured on (traffic is reported only
 # while the source is unchanged).
 TRAFFIC = {
-    # ncu dram bytes (read + write) of the sparse reuse launch of the 40-head
-    # large workload, one-pass capture at full size (mean of the eight timed
-    # launches of `bench.py --steps 2 --warmup 1 --no-e2e --no-cpu-baseline`)
-    "attn.cu": {"sha": "1e2afdf3b6cf", "bytes_per_launch": 7190463584},
+    # ncu dram bytes (read + write) of the sparse reuse launch, captured on the
+    # 4-head large workload (mean of two launches of `bench.py --heads 4
+    # --steps 1 --warmup 1 --no-e2e --no-cpu-baseline --no-workloads`), times
+    # 10 for the 40-head launch: heads are independent and the grid scales
+    # with them
+    "attn.cu": {"sha": "6dbdbda25108", "bytes_per_launch": 7252938240},
 }
 
 
@@ -74,6 +76,18 @@ def reduce_max_over_ranks(vals, dist, device):
     if dist is not None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def depths_of(G: int) -> int:
+    """Tree depths of the PDDP grouping: ceil(log2 G)."""
+    return max(0, math.ceil(math.log2(G))) if G > 1 else 0
+
+
+def pddp_bytes(BH: int, N: int, D: int, G: int) -> float:
+    """Algorithmic HBM bytes of the PDDP grouping: per depth, every head's
+    rows read twice (moments and projection, bf16) plus the index traffic
+    (positions read, keys written and read back, 4 bytes each)."""
+    return depths_of(G) * (2 * 2.0 * BH * N * D + 3 * 4.0 * BH * N)
 
 
 def sum_over_ranks(x, dist, device):
@@ -463,7 +477,15 @@ def run_gpu(args, w, K, rank, world, dist):
                        "frac": tflops(flops_dense, t_dense) / peak},
         "group_mass+topk": {"ms": stage_ms["select"],
                             "tflops_qk": tflops(flops_dense / 2, stage_ms["select"])},
-        "pddp": {"ms": stage_ms["pddp"]},
+        # algorithmic bytes per depth: Q read twice (moments, projection) and
+        # the index traffic (perm read, keys written and read), 2-D x 2 + 3 x 4
+        # bytes per token and head
+        "pddp": {"ms": stage_ms["pddp"], "depths": depths_of(G),
+                 "algorithmic_gb": pddp_bytes(BH, w.N, w.D, G) / 1e9,
+                 "gbs": pddp_bytes(BH, w.N, w.D, G) / (stage_ms["pddp"] * 1e-3) / 1e9,
+                 "frac": pddp_bytes(BH, w.N, w.D, G) / (stage_ms["pddp"] * 1e-3) / 1e9
+                 / float(peaks.get("hbm_gbs", 6800.0)),
+                 "peak": "hbm_gbs (" + peak_kind + ")"},
     }
     depths = max(0, math.ceil(math.log2(G))) if G > 1 else 0
     # mcs_select passes the heads through the workspace in chunks; each chunk
