@@ -69,10 +69,19 @@ def test_anchor_and_reuse_are_layout_independent(B, H, N, D, C, K):
         pidx = torch.empty(B, H, p.G, pb.K, dtype=torch.int32, device="cuda")
         mcs.mcs_pooled_block_select(pb, qa, ka, perm, blk, pidx,
                                     mcs.empty_workspace(mcs.mcs_block_workspace(pb, blk)))
+        extra = {}
+        if mcs.mcs_pair_bytes(p):  # C = 64: the sibling-pair path
+            pairs = mcs.empty_pairs(p)
+            mcs.mcs_pair_lists(p, idx, pairs)
+            pout = torch.empty_like(qa)
+            mcs.mcs_sparse_attn_pairs(p, cv(q1), cv(k1), cv(v1), perm, pairs, resid, pout)
+            prec = torch.empty_like(qa)
+            mcs.mcs_sparse_attn_pairs_record(p, qa, ka, va, perm, pairs, dense, prec)
+            extra = dict(pout=back(pout), prec=back(prec))  # (the lists come from idx)
         assert mcs.mcs_device_status() == 0
         res[layout] = dict(perm=perm, idx=idx, dense=back(dense), lse=lse, resid=back(resid),
                            ret=ret, out=back(out), perm2=perm2, perm3=perm3, mass=mass,
-                           rec=back(rec), plain=back(plain), pidx=pidx)
+                           rec=back(rec), plain=back(plain), pidx=pidx, **extra)
     a, b = res[mcs.LAYOUT_BHND], res[mcs.LAYOUT_BNHD]
     for name in a:
         same(a[name], b[name], name)

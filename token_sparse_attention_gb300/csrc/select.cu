@@ -43,7 +43,11 @@ __device__ __forceinline__ uint32_t mass_digit(uint32_t bits) {
   return min(bits >> 20, static_cast<uint32_t>(kHistBins - 1));
 }
 
-template <int D, int CQ>
+// GP groups per CTA: 1, or 2 sibling C = 64 groups sharing one 128-query
+// tile (a 64-column MMA costs nearly as much as a 128-column one, and the K
+// tiles are then loaded once for both groups); each group keeps its own mass
+// row and histogram.
+template <int D, int CQ, int GP>
 struct MassLayout {
   static constexpr int kSub = D / 64;
   static constexpr int kQSub = CQ * 128;        // CQ rows x 128 B
@@ -57,10 +61,11 @@ struct MassLayout {
   static constexpr int kOnes = kK0 + 2 * kKStage;
   static constexpr int kQb = kOnes + 128 * 32;
   static constexpr int kHist = kQb + CQ * 32;            // mass histogram (kHistBins words)
-  static constexpr int kBars = kHist + kHistBins * 4;
+  static constexpr int kBars = kHist + GP * kHistBins * 4;
   static constexpr int kUsed = kBars + 128 + 1024;
   // at most two CTAs per SM (TMEM: 2 x 256 columns)
   static constexpr int kSmem = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
+  static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
   static constexpr int kTmemCols = 2 * CQ < 32 ? 32 : 2 * CQ;
 };
 
@@ -77,11 +82,11 @@ __device__ __forceinline__ void drain_wait_m(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D, int CQ>
+template <int D, int CQ, int GP>
 __global__ void __launch_bounds__(kMassThreads, 2)
     group_mass_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const MassArgs a) {
-  using L = MassLayout<D, CQ>;
+  using L = MassLayout<D, CQ, GP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -101,7 +106,9 @@ __global__ void __launch_bounds__(kMassThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int g = blockIdx.x;
+  const int g = blockIdx.x * GP;             // the CTA's first group
+  const int ng = min(GP, a.G - g);           // its groups (the last CTA may have one)
+  const int qrows = ng * a.C;                // their query rows, adjacent in perm
   const int hc = blockIdx.y;          // head within the chunk
   const int bh = a.head0 + hc;        // global head
   const int ntiles = (a.N + 127) / 128;
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
     *reinterpret_cast<uint4*>(sones + core + 128) = make_uint4(0u, 0u, 0u, 0u);
     if (r < CQ) {
       constexpr float kLog2e = 1.4426950408889634f;
-      const int p = (r < a.C) ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g) * a.C + r) : -1;
+      const int p = (r < qrows) ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g) * a.C + r) : -1;
       float b = -1e30f;
       if (p >= 0 && p < a.N)
         b = -(__ldg(a.lse + static_cast<size_t>(bh) * a.N + p) * kLog2e) / a.scale_log2;
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kMassThreads, 2)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int p = 4 * r4 + i;
-        int t = (p < a.C) ? __ldg(perm_g + p) : 0;
+        int t = (p < qrows) ? __ldg(perm_g + p) : 0;
         if (t < 0) t = 0;
         if (t >= a.N) { bad = true; t = 0; }
         r[i] = rm.rbase + t * rm.rstride;
@@ -243,36 +250,45 @@ __global__ void __launch_bounds__(kMassThreads, 2)
     const int t = threadIdx.x;  // 0..127: KV row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     if (a.hist != nullptr)
-      for (int b = t; b < kHistBins; b += 128) shist[b] = 0;
+      for (int b = t; b < GP * kHistBins; b += 128) shist[b] = 0;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const float sl2 = a.scale_log2;
     float* mass_row = a.mass + (static_cast<size_t>(hc) * a.G + g) * a.N;
+    constexpr int kCols = CQ / GP;  // score columns (queries) of one group
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       if (!warp_wait_m(s_full + st, (j >> 1) & 1, abort_flag, a.status)) break;
       tc_fence_after();
-      float acc = 0.f;
+      float acc[GP];
+#pragma unroll
+      for (int gi = 0; gi < GP; ++gi) acc[gi] = 0.f;
 #pragma unroll
       for (int c = 0; c < CQ / 32; ++c) {
         uint32_t s[32];
         tmem_ld32(tmem + st * CQ + lane_off + c * 32, s);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc += ex2(__uint_as_float(s[i]) * sl2);
+        for (int i = 0; i < 32; ++i) acc[(c * 32) / kCols] += ex2(__uint_as_float(s[i]) * sl2);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + st);
       const int jrow = j * 128 + t;
       if (jrow < a.N) {
-        mass_row[jrow] = acc;
-        if (a.hist != nullptr) atomicAdd(&shist[mass_digit(__float_as_uint(acc))], 1u);
+#pragma unroll
+        for (int gi = 0; gi < GP; ++gi) {
+          if (gi < ng) {
+            mass_row[static_cast<size_t>(gi) * a.N + jrow] = acc[gi];
+            if (a.hist != nullptr)
+              atomicAdd(&shist[gi * kHistBins + mass_digit(__float_as_uint(acc[gi]))], 1u);
+          }
+        }
       }
     }
     if (a.hist != nullptr) {
       asm volatile("bar.sync 1, 128;" ::: "memory");
       uint32_t* hist_row = a.hist + (static_cast<size_t>(hc) * a.G + g) * kHistBins;
-      for (int b = t; b < kHistBins; b += 128) hist_row[b] = shist[b];
+      for (int b = t; b < ng * kHistBins; b += 128) hist_row[b] = shist[b];
     }
   }
 
@@ -282,14 +298,14 @@ __global__ void __launch_bounds__(kMassThreads, 2)
   if (warp == 5) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int D, int CQ>
+template <int D, int CQ, int GP>
 cudaError_t launch_mass_one(const CUtensorMap* tq, const CUtensorMap* tk, const MassArgs& a,
                             int heads, cudaStream_t stream) {
-  auto kern = group_mass_kernel<D, CQ>;
-  const int smem = MassLayout<D, CQ>::kSmem;
+  auto kern = group_mass_kernel<D, CQ, GP>;
+  const int smem = MassLayout<D, CQ, GP>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.G, heads), kMassThreads, smem, stream>>>(*tq, *tk, a);
+  kern<<<dim3((a.G + GP - 1) / GP, heads), kMassThreads, smem, stream>>>(*tq, *tk, a);
   return cudaGetLastError();
 }
 
@@ -669,10 +685,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 
 cudaError_t launch_group_mass(int D, const CUtensorMap* tq, const CUtensorMap* tk,
                               const MassArgs& a, int heads, cudaStream_t stream) {
-  if (D == 128 && a.C == 128) return launch_mass_one<128, 128>(tq, tk, a, heads, stream);
-  if (D == 128 && a.C == 64) return launch_mass_one<128, 64>(tq, tk, a, heads, stream);
-  if (D == 64 && a.C == 128) return launch_mass_one<64, 128>(tq, tk, a, heads, stream);
-  if (D == 64 && a.C == 64) return launch_mass_one<64, 64>(tq, tk, a, heads, stream);
+  // C = 64, D = 64: two sibling groups per CTA (at D = 128 the paired
+  // layout's shared memory would allow only one CTA per SM)
+  if (D == 128 && a.C == 128) return launch_mass_one<128, 128, 1>(tq, tk, a, heads, stream);
+  if (D == 128 && a.C == 64) return launch_mass_one<128, 64, 1>(tq, tk, a, heads, stream);
+  if (D == 64 && a.C == 128) return launch_mass_one<64, 128, 1>(tq, tk, a, heads, stream);
+  if (D == 64 && a.C == 64) return launch_mass_one<64, 128, 2>(tq, tk, a, heads, stream);
   return cudaErrorInvalidValue;
 }
 
