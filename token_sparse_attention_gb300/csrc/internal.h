@@ -136,15 +136,11 @@ cudaError_t launch_pair_union(const int32_t* idx, int BH, int G, int K, int N, v
 
 // Device address of the library's status word (for kernels' status argument).
 cudaError_t device_status_word(unsigned** out);
-// 2-D gather tensor map over `rows` bf16 rows of D columns (box {64, 1}).
-bool encode_gather_map(CUtensorMap* m, const void* base, long long rows, int D);
-
 size_t pddp_workspace_bytes(int BH, int N, int D, int C);
 // Groups heads [head0, head0 + BH) of q (all B*H heads, in `layout`, H heads
-// per batch entry); tq_gather covers every row of q.  perm_out points at the
-// first of those heads' perm rows.
-cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int layout, int H,
-                        int head0, int BH, int N, int D, int C, int iters, int32_t* perm_out,
-                        void* ws, size_t ws_bytes, unsigned* status, cudaStream_t stream);
+// per batch entry).  perm_out points at the first of those heads' perm rows.
+cudaError_t launch_pddp(const __nv_bfloat16* q, int layout, int H, int head0, int BH, int N,
+                        int D, int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,
+                        unsigned* status, cudaStream_t stream);
 
 }  // namespace mcs

@@ -238,9 +238,6 @@ mcs_status check_params(const mcs_params* p, bool need_k) { return check_shape(p
 cudaError_t device_status_word(unsigned** out) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_mcs_status);
 }
-bool encode_gather_map(CUtensorMap* m, const void* base, long long rows, int D) {
-  return make_gather_map(m, base, 1, static_cast<int>(rows), D);
-}
 }  // namespace mcs
 
 extern "C" {
@@ -298,14 +295,10 @@ mcs_status mcs_group(const mcs_params* p, const void* q, int32_t* perm, void* ws
   const size_t need = mcs_group_workspace(p);
   if (ws_bytes < need || (need > 0 && ws == nullptr) || !aligned16(ws)) return MCS_ERR_WORKSPACE;
   const int BH = p->B * p->H;
-  CUtensorMap tq;
-  if (!make_gather_map(&tq, q, BH, p->N, p->D))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(gather)");
   unsigned* st;
   if ((s = status_ptr(&st)) != MCS_OK) return s;
-  cudaError_t e = mcs::launch_pddp(static_cast<const __nv_bfloat16*>(q), &tq, p->layout, p->H, 0, BH,
-                                   p->N, p->D, p->C,
-                                   iters_of(p), perm, ws, ws_bytes, st, stream);
+  cudaError_t e = mcs::launch_pddp(static_cast<const __nv_bfloat16*>(q), p->layout, p->H, 0, BH,
+                                   p->N, p->D, p->C, iters_of(p), perm, ws, ws_bytes, st, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pddp launch");
   return MCS_OK;
 }

@@ -52,15 +52,11 @@ extern "C" mcs_status mcs_group_noalloc(const mcs_params* p, const void* q, int3
   if ((e = mcs::device_status_word(&status)) != cudaSuccess)
     return mcs::record_cuda_error(e, "status word");
 
-  // The kernels address q's rows by global head (either layout), so every
-  // batch uses the one gather map over all rows.
+  // The kernels address q's rows by global head (either layout).
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
-  CUtensorMap tq;
-  if (!mcs::encode_gather_map(&tq, qb, static_cast<long long>(BH) * N, D))
-    return mcs::record_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(noalloc gather)");
   for (int h0 = 0; h0 < BH; h0 += batch) {
     const int hc = BH - h0 < batch ? BH - h0 : batch;
-    e = mcs::launch_pddp(qb, &tq, p->layout, p->H, h0, hc, N, D, C, iters,
+    e = mcs::launch_pddp(qb, p->layout, p->H, h0, hc, N, D, C, iters,
                          perm + static_cast<size_t>(h0) * G * C, scratch, kNoallocScratchBytes,
                          status, stream);
     if (e != cudaSuccess) return mcs::record_cuda_error(e, "noalloc grouping launch");

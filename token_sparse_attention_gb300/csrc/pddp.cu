@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int D>
-cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int layout, int H, int head0,
+cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
                      int BH, int N, int C, int iters, int32_t* perm_out, void* ws,
                      unsigned* status, cudaStream_t stream) {
   const WsLayout w = ws_layout(BH, N, D, C);
@@ -796,16 +796,13 @@ cudaError_t run_pddp(const __nv_bfloat16* q, const CUtensorMap* tq, int layout, 
 
 size_t pddp_workspace_bytes(int BH, int N, int D, int C) { return ws_layout(BH, N, D, C).total; }
 
-cudaError_t launch_pddp(const __nv_bfloat16* q, const CUtensorMap* tq_gather, int layout, int H,
-                        int head0, int BH, int N, int D, int C, int iters, int32_t* perm_out,
-                        void* ws, size_t ws_bytes, unsigned* status, cudaStream_t stream) {
+cudaError_t launch_pddp(const __nv_bfloat16* q, int layout, int H, int head0, int BH, int N,
+                        int D, int C, int iters, int32_t* perm_out, void* ws, size_t ws_bytes,
+                        unsigned* status, cudaStream_t stream) {
   if (ws_bytes < pddp_workspace_bytes(BH, N, D, C)) return cudaErrorInvalidValue;
   if (D == 128)
-    return run_pddp<128>(q, tq_gather, layout, H, head0, BH, N, C, iters, perm_out, ws, status,
-                         stream);
-  if (D == 64)
-    return run_pddp<64>(q, tq_gather, layout, H, head0, BH, N, C, iters, perm_out, ws, status,
-                        stream);
+    return run_pddp<128>(q, layout, H, head0, BH, N, C, iters, perm_out, ws, status, stream);
+  if (D == 64) return run_pddp<64>(q, layout, H, head0, BH, N, C, iters, perm_out, ws, status, stream);
   return cudaErrorInvalidValue;
 }
 
