@@ -23,11 +23,14 @@ def _lib():
 
 def _buffers(p, q):
     G = p.G
-    return dict(perm=torch.empty(p.B, p.H, G * p.C, dtype=torch.int32, device="cuda"),
-                idx=torch.empty(p.B, p.H, G, p.K, dtype=torch.int32, device="cuda"),
-                dense=torch.empty_like(q), lse=torch.empty(p.B, p.H, p.N, device="cuda"),
-                res=torch.empty_like(q), ret=torch.empty(p.B, p.H, G, device="cuda"),
-                out=torch.empty_like(q))
+    b = dict(perm=torch.empty(p.B, p.H, G * p.C, dtype=torch.int32, device="cuda"),
+             idx=torch.empty(p.B, p.H, G, p.K, dtype=torch.int32, device="cuda"),
+             dense=torch.empty_like(q), lse=torch.empty(p.B, p.H, p.N, device="cuda"),
+             res=torch.empty_like(q), ret=torch.empty(p.B, p.H, G, device="cuda"),
+             out=torch.empty_like(q))
+    if mcs.mcs_pair_bytes(p):
+        b["pout"] = torch.empty_like(q)
+    return b
 
 
 def _run(p, q0, k0, v0, q1, k1, v1, b):
@@ -35,6 +38,10 @@ def _run(p, q0, k0, v0, q1, k1, v1, b):
     mcs.mcs_anchor_select(p, q0, k0, v0, b["perm"], b["idx"], b["dense"], b["lse"], b["res"],
                           ws, retained=b["ret"])
     mcs.mcs_sparse_attn(p, q1, k1, v1, b["perm"], b["idx"], b["res"], b["out"])
+    if "pout" in b:  # C = 64: each rank builds its heads' sibling-pair lists
+        pairs = mcs.empty_pairs(p)
+        mcs.mcs_pair_lists(p, b["idx"], pairs)
+        mcs.mcs_sparse_attn_pairs(p, q1, k1, v1, b["perm"], pairs, b["res"], b["pout"])
 
 
 @pytest.mark.parametrize("world", [2, 3])
