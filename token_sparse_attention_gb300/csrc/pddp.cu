@@ -210,10 +210,13 @@ __global__ void __launch_bounds__(kMomThreads, 3)
     const int pw = warp - 4;
     const int sub = lane / kSegs, seg = lane % kSegs;
     bool bad = false;
+    // the token of the lane's row of tile j + 1 is loaded while tile j is copied
+    int tnext = pw * 32 + lane < rows ? __ldg(pos + pw * 32 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       const int rr = j * 128 + pw * 32 + lane;
-      int t = rr < rows ? __ldg(pos + rr) : -1;
+      int t = tnext;
+      if (j + 1 < ntiles) tnext = rr + 128 < rows ? __ldg(pos + rr + 128) : -1;
       if (t >= N || (rr < rows && t < 0)) { bad = true; t = -1; }
       const int myrow = t < 0 ? -1 : rm.rbase + t * rm.rstride;
       if (j >= 2) {
@@ -341,29 +344,69 @@ __global__ void __launch_bounds__(kMomThreads, 3)
 
 // ---------------------------------------------------------------- power iteration
 
+// Nodes of more than kChunkRows rows leave one partial (X^T X, column sums)
+// per chunk.  Nodes of at least kReduceChunks chunks have them summed into
+// chunk 0 here, in chunk order, one float4 of the partial per thread, so that
+// the power kernel (one CTA per node) reads a single partial; the power
+// kernel sums fewer chunks itself, in the same order.
+constexpr int kReduceThreads = 256;
+constexpr int kReduceChunks = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kReduceThreads)
+    pddp_reduce_kernel(float* __restrict__ partials, int N, int C, int depth, int slots,
+                       int max_chunks) {
+  constexpr int DD = D * D + D;
+  static_assert(DD % 4 == 0, "partials are float4 vectors");
+  const int q4 = blockIdx.x * kReduceThreads + threadIdx.x;
+  const int slot = blockIdx.y, bh = blockIdx.z;
+  if (q4 * 4 >= DD) return;
+  const Node nd = node_at(N, C, depth, slot);
+  const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
+  if ((nd.n + C - 1) / C <= 1 || nchunks < kReduceChunks) return;
+  float4* base = reinterpret_cast<float4*>(partials + (size_t)(bh * slots + slot) * max_chunks * DD);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const float4 x = __ldg(base + (size_t)ch * (DD / 4) + q4);
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+  }
+  base[q4] = acc;
+}
+
 constexpr int kPowThreads = 256;
 
-// One CTA per node.  Thread t owns row a = t / TPR of the node's covariance
-// and the contiguous columns [part*SEG, (part+1)*SEG) of it (SEG = D / TPR),
-// kept in registers as packed fp32 pairs for every iteration; an iteration
-// reads only the current vector from shared memory (16-byte broadcast loads)
-// and multiplies with packed f32x2 FMAs.  The matrix is first divided by its
-// trace (largest eigenvalue <= 1, so the iterate cannot overflow), and the
-// iterate is normalised after the first step, every kNormEvery steps and at
-// the end instead of every step: power iteration's direction does not depend
-// on the scale of the iterate, and a node whose covariance sends the start
-// vector to zero is caught at the first step (it keeps the start vector).
-// One block barrier per step.  (Re-reading the D x D matrix from shared
-// memory every iteration made the deep tree levels, with thousands of nodes,
-// shared-memory bound.)
+// One CTA per node.  The D x D covariance is cut into 16 x 16 blocks of
+// R = D/16 rows by 4*J = D/16 columns: half-warp h of warp w holds row block
+// 2w + h, its lane c the columns [64j + 4c, 64j + 4c + 4) of those rows
+// (j < J), all in registers as packed fp32 pairs for every iteration.  A step
+// reads J 16-byte pieces of the iterate from shared memory, multiplies with
+// packed f32x2 FMAs (R partial dot products per thread), and a reduce-scatter
+// across the 16 lanes of the half-warp (shuffles) leaves each row's sum in
+// 2 (D = 128) or 4 (D = 64) lanes, one of which stores it.  A lane holds its
+// rows in the order i ^ sigma (sigma from its lane bits), so that at every
+// halving level it keeps the first half and its partner's second half is the
+// same rows: no selects.  The matrix is first divided by
+// its trace (largest eigenvalue <= 1, so the iterate cannot overflow), and
+// the iterate is normalised after the first step, every kNormEvery steps and
+// at the end instead of every step: power iteration's direction does not
+// depend on the scale of the iterate, and a node whose covariance sends the
+// start vector to zero is caught at the first step (it keeps the start
+// vector).  One block barrier per step.  (One covariance row per thread pair
+// made every thread read D/2 iterate entries per step: the shared-memory
+// pipe, not the FMAs, set the pace of the deep levels.)
 template <int D>
 __global__ void __launch_bounds__(kPowThreads, 2)
     pddp_power_kernel(const float* __restrict__ partials, int N, int C, int depth, int slots,
                       int max_chunks, int iters, float* __restrict__ nodevec) {
-  constexpr int TPR = kPowThreads / D;  // threads per row: 2 (D=128) or 4 (D=64)
-  constexpr int SEG = D / TPR;          // columns per thread: 64 or 16
+  constexpr int R = D / 16;  // rows per thread: 8 (D = 128) or 4 (D = 64)
+  constexpr int J = D / 64;  // 4-column pieces per thread: 2 or 1
   constexpr int kNormEvery = 8;
-  static_assert(SEG % 4 == 0 && 32 % TPR == 0, "row segments are float4 vectors in one warp");
+  constexpr int DD = D * D + D;  // one partial: X^T X, then the column sums
+  static_assert(kPowThreads == 256 && (D == 64 || D == 128), "16 x 16 blocks over 8 warps");
   __shared__ __align__(16) float s[D];
   __shared__ __align__(16) float vb[2][D];  // the iterate, double-buffered
   __shared__ float red[kPowThreads / 32];
@@ -371,42 +414,78 @@ __global__ void __launch_bounds__(kPowThreads, 2)
   const int slot = blockIdx.x, bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
   if ((nd.n + C - 1) / C <= 1) return;
-  const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int a = tid / TPR, part = tid % TPR, b0 = part * SEG;
-  constexpr int DD = D * D + D;  // one chunk's partials: X^T X, then the column sums
-  const float* base = partials + (size_t)(bh * slots + slot) * max_chunks * DD;
-  // this thread's covariance segment (packed pairs) and (first D threads)
-  // the column sums, summed over the node's chunks in chunk order
-  uint64_t cp[SEG / 2];
+  const int cb = lane & 15, r0 = (wid * 2 + (lane >> 4)) * R;
+  // sigma: the row offset a lane's reduce-scatter ends on; wmask: the lane
+  // bits of the plain butterfly levels (the lane stores if they are zero)
+  int sigma = 0, wmask = 0;
+  {
+    int len = R;
 #pragma unroll
-  for (int k = 0; k < SEG / 2; ++k) cp[k] = 0ull;
-  float sacc = 0.f, dacc = 0.f;
-  for (int ch = 0; ch < nchunks; ++ch) {
-    const float* pc = base + (size_t)ch * DD;
-    const ulonglong2* row = reinterpret_cast<const ulonglong2*>(pc + a * D + b0);
-#pragma unroll
-    for (int k4 = 0; k4 < SEG / 4; ++k4) {
-      const ulonglong2 x = __ldg(row + k4);
-      cp[2 * k4] = f2_add(cp[2 * k4], x.x);
-      cp[2 * k4 + 1] = f2_add(cp[2 * k4 + 1], x.y);
+    for (int m = 8; m >= 1; m >>= 1) {
+      if (len > 1) {
+        len >>= 1;
+        if (lane & m) sigma += len;
+      } else {
+        wmask |= m;
+      }
     }
-    if (tid < D) sacc += __ldg(pc + D * D + tid);
-    if (part == 0) dacc += __ldg(pc + a * D + a);  // the diagonal, for the trace
+  }
+  const float* pc = partials + (size_t)(bh * slots + slot) * max_chunks * DD;
+  const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
+  const int nsum = nchunks >= kReduceChunks ? 1 : nchunks;  // chunk 0 holds the sum, or sum here
+  uint64_t cp[R][2 * J];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const ulonglong2 x =
+          __ldg(reinterpret_cast<const ulonglong2*>(pc + (r0 + (i ^ sigma)) * D + 64 * j + 4 * cb));
+      cp[i][2 * j] = x.x;
+      cp[i][2 * j + 1] = x.y;
+    }
+  float diag = 0.f, colsum = 0.f;
+  if (tid < D) {
+    colsum = __ldg(pc + D * D + tid);
+    diag = __ldg(pc + tid * D + tid);
+  }
+#pragma unroll 1
+  for (int ch = 1; ch < nsum; ++ch) {
+    const float* pk = pc + (size_t)ch * DD;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const ulonglong2 x = __ldg(
+            reinterpret_cast<const ulonglong2*>(pk + (r0 + (i ^ sigma)) * D + 64 * j + 4 * cb));
+        cp[i][2 * j] = f2_add(cp[i][2 * j], x.x);
+        cp[i][2 * j + 1] = f2_add(cp[i][2 * j + 1], x.y);
+      }
+    if (tid < D) {
+      colsum += __ldg(pk + D * D + tid);
+      diag += __ldg(pk + tid * D + tid);
+    }
   }
   if (tid < D) {
-    s[tid] = sacc;
+    s[tid] = colsum;
     vb[0][tid] = rsqrtf(static_cast<float>(D));
   }
   __syncthreads();
   const float inv_n = 1.f / static_cast<float>(nd.n);
-  const float sa = s[a] * inv_n;
-  const uint64_t nsa = f2_pack(-sa, -sa);
+  // Cov = X^T X - s s^T / n
 #pragma unroll
-  for (int k = 0; k < SEG / 2; ++k)
-    cp[k] = f2_fma(nsa, f2_pack(s[b0 + 2 * k], s[b0 + 2 * k + 1]), cp[k]);  // Cov = X^T X - s s^T / n
-  float diag = part == 0 ? dacc - sa * s[a] : 0.f;
+  for (int i = 0; i < R; ++i) {
+    const float sa = s[r0 + (i ^ sigma)] * inv_n;
+    const uint64_t nsa = f2_pack(-sa, -sa);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float4 sb = *reinterpret_cast<const float4*>(s + 64 * j + 4 * cb);
+      cp[i][2 * j] = f2_fma(nsa, f2_pack(sb.x, sb.y), cp[i][2 * j]);
+      cp[i][2 * j + 1] = f2_fma(nsa, f2_pack(sb.z, sb.w), cp[i][2 * j + 1]);
+    }
+  }
   // trace of Cov, then Cov / trace
+  if (tid < D) diag -= s[tid] * inv_n * s[tid];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) diag += __shfl_xor_sync(0xffffffffu, diag, o);
   if (lane == 0) red[wid] = diag;
@@ -417,24 +496,44 @@ __global__ void __launch_bounds__(kPowThreads, 2)
   const float inv_tr = tr > 0.f ? 1.f / tr : 1.f;
   const uint64_t itr2 = f2_pack(inv_tr, inv_tr);
 #pragma unroll
-  for (int k = 0; k < SEG / 2; ++k) cp[k] = f2_fma(cp[k], itr2, 0ull);
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int k = 0; k < 2 * J; ++k) cp[i][k] = f2_fma(cp[i][k], itr2, 0ull);
+  const bool writer = (lane & wmask) == 0;
   int cur = 0;
   for (int it = 0; it < iters; ++it) {
-    uint64_t acc0 = 0ull, acc1 = 0ull;
-    const ulonglong2* v2 = reinterpret_cast<const ulonglong2*>(vb[cur] + b0);
+    ulonglong2 vv[J];
 #pragma unroll
-    for (int k4 = 0; k4 < SEG / 4; ++k4) {
-      const ulonglong2 x = v2[k4];
-      acc0 = f2_fma(cp[2 * k4], x.x, acc0);
-      acc1 = f2_fma(cp[2 * k4 + 1], x.y, acc1);
+    for (int j = 0; j < J; ++j)
+      vv[j] = *reinterpret_cast<const ulonglong2*>(vb[cur] + 64 * j + 4 * cb);
+    float acc[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      uint64_t a2 = 0ull;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        a2 = f2_fma(cp[i][2 * j], vv[j].x, a2);
+        a2 = f2_fma(cp[i][2 * j + 1], vv[j].y, a2);
+      }
+      float lo, hi;
+      f2_unpack(a2, lo, hi);
+      acc[i] = lo + hi;
     }
-    float a0, a1, a2, a3;
-    f2_unpack(acc0, a0, a1);
-    f2_unpack(acc1, a2, a3);
-    float acc = (a0 + a1) + (a2 + a3);
+    // reduce-scatter over the half-warp: halve the row set per level while
+    // more than one row is left, then plain butterfly sums
+    int len = R;
 #pragma unroll
-    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (part == 0) vb[cur ^ 1][a] = acc;
+    for (int m = 8; m >= 1; m >>= 1) {
+      if (len > 1) {
+        const int half = len >> 1;
+#pragma unroll
+        for (int k = 0; k < half; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k + half], m);
+        len = half;
+      } else {
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], m);
+      }
+    }
+    if (writer) vb[cur ^ 1][r0 + sigma] = acc[0];
     __syncthreads();
     cur ^= 1;
     if (it == 0 || (it + 1) % kNormEvery == 0 || it == iters - 1) {
@@ -459,12 +558,27 @@ __global__ void __launch_bounds__(kPowThreads, 2)
   }
   __syncthreads();
   const float* v = vb[cur];
-  if (tid == 0) {
-    int best = 0;
-    float bv = fabsf(v[0]);
-    for (int i = 1; i < D; ++i)
-      if (fabsf(v[i]) > bv) { bv = fabsf(v[i]); best = i; }
-    lead = best;
+  if (wid == 0) {  // largest |v_d|, lowest d on ties
+    float bv = -1.f;
+    int bi = 0;
+#pragma unroll
+    for (int k = lane; k < D; k += 32) {
+      const float a = fabsf(v[k]);
+      if (a > bv) {
+        bv = a;
+        bi = k;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > bv || (ob == bv && oi < bi)) {
+        bv = ob;
+        bi = oi;
+      }
+    }
+    if (lane == 0) lead = bi;
   }
   __syncthreads();
   const float sign = v[lead] < 0.f ? -1.f : 1.f;
@@ -774,6 +888,12 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
     pddp_moments_kernel<D><<<dim3(chunks, slots, BH), kMomThreads, msmem, stream>>>(
         q, pa, N, C, d, slots, chunks, partials, status, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (chunks >= kReduceChunks) {
+      constexpr int kQ4 = (D * D + D) / 4;
+      pddp_reduce_kernel<D><<<dim3((kQ4 + kReduceThreads - 1) / kReduceThreads, slots, BH),
+                              kReduceThreads, 0, stream>>>(partials, N, C, d, slots, chunks);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     pddp_power_kernel<D><<<dim3(slots, BH), kPowThreads, psmem, stream>>>(partials, N, C, d, slots,
                                                                           chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
