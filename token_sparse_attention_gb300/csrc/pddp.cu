@@ -16,18 +16,20 @@
 // nodes at once; between depths only the permutation array (token index per
 // position) moves, nodes being contiguous position ranges.
 //
-// One depth = four launches:
+// One depth = four to six launches:
 //   pddp_moments   per (head, node, chunk of <= kChunkRows rows): the rows,
 //                  gathered in position order with 16-byte cp.async into a
 //                  swizzled two-stage ring; X^T X on tcgen05 (A = X^T, B = X,
 //                  both MN-major views of the same tile), fp32 in TMEM; the
 //                  column sums on the CUDA cores (16-byte shared loads)
-//   pddp_power     per (head, node): sum the chunk partials in fixed order,
+//   pddp_reduce    (nodes of many chunks) sum the chunk partials in chunk order
+//   pddp_power     per (head, node): (sum a few chunk partials in chunk order)
 //                  Cov = X^T X - s s^T / n, then `iters` steps v <- Cov v/|Cov v|
 //                  from (1,..,1)/sqrt(D); sign: largest |v_d| positive
 //   pddp_project   per position: t = (x - mu).v, key = (ordered bits of t, token)
 //   pddp_split     per (head, node): radix-select the C*floor(g/2)-th smallest
-//                  key, stable partition of the positions (leaves are copied)
+//                  key, stable partition of the positions; one CTA per big node,
+//                  one warp per small node (a new leaf is copied once)
 // and finally pddp_finalize sorts each group's indices ascending and pads the
 // short group with -1.
 #include "internal.h"
@@ -47,12 +49,16 @@ struct Node {
 
 // Node of `slot` at `depth` (slot's bits from the most significant one are
 // the left(0)/right(1) path).  n == 0: no node (a leaf reached earlier).
-__host__ __device__ inline Node node_at(int N, int C, int depth, int slot) {
+// *stale (optional): the walk passed a leaf above `depth` (the node is that
+// leaf, carried down along its 0 path).
+__host__ __device__ inline Node node_at(int N, int C, int depth, int slot,
+                                        bool* stale = nullptr) {
   Node nd{0, N};
   for (int b = depth - 1; b >= 0; --b) {
     const int bit = (slot >> b) & 1;
     const int g = (nd.n + C - 1) / C;
     if (g <= 1) {
+      if (stale) *stale = true;
       if (bit) nd.n = 0;
       if (nd.n == 0) return nd;
       continue;
@@ -703,8 +709,20 @@ __global__ void __launch_bounds__(kProjThreads)
 }
 
 // ---------------------------------------------------------------- select + partition
+//
+// Each splitting node finds T, the C*floor(g/2)-th smallest of its keys (keys
+// are distinct: the token is the low word), by radix select over 8-bit digits
+// from the top, then partitions its positions stably: key <= T left, the rest
+// right.  Nodes of more than kSmallNode rows take one CTA each and stream
+// their keys from global memory (kUnroll independent loads in flight per
+// thread); smaller nodes take one warp each, with the keys in shared memory
+// and no block barrier.  A leaf is copied to the output buffer once, at the
+// depth where it appears; from then on both buffers hold its final positions.
 
 constexpr int kSplitThreads = 512;
+constexpr int kSmallNode = 1024;
+constexpr int kSmallWarps = 4;
+constexpr int kUnroll = 4;
 
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -740,16 +758,12 @@ __global__ void __launch_bounds__(kSplitThreads)
   __shared__ uint32_t sel_digit, sel_below;
   const int slot = blockIdx.x, bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
-  if (nd.n == 0) return;
+  const int g = (nd.n + C - 1) / C;
+  if (g <= 1 || nd.n <= kSmallNode) return;  // leaves and small nodes: the warp path
   const int tid = threadIdx.x;
   const int32_t* in = perm_in + (size_t)bh * N + nd.start;
   int32_t* out = perm_out + (size_t)bh * N + nd.start;
-  const int g = (nd.n + C - 1) / C;
-  if (g <= 1) {
-    for (int i = tid; i < nd.n; i += kSplitThreads) out[i] = in[i];
-    return;
-  }
-  const int nl = C * (g / 2);
+  const int n = nd.n, nl = C * (g / 2);
   const uint64_t* kk = keys + (size_t)bh * N + nd.start;
   // radix select of the nl-th smallest key, 8 bits at a time from the top
   uint64_t prefix = 0, mask = 0;
@@ -758,9 +772,17 @@ __global__ void __launch_bounds__(kSplitThreads)
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += kSplitThreads) hist[b] = 0;
     __syncthreads();
-    for (int i = tid; i < nd.n; i += kSplitThreads) {
-      const uint64_t k = kk[i];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    for (int i0 = tid; i0 < n; i0 += kUnroll * kSplitThreads) {
+      uint64_t k[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = i0 + u * kSplitThreads;
+        k[u] = i < n ? kk[i] : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (i0 + u * kSplitThreads < n && (k[u] & mask) == prefix)
+          atomicAdd(&hist[(k[u] >> shift) & 255u], 1u);
     }
     __syncthreads();
     uint32_t mine = tid < 256 ? hist[tid] : 0u;
@@ -788,15 +810,22 @@ __global__ void __launch_bounds__(kSplitThreads)
   // stable partition by position: key <= T left, else right.  Warp w owns
   // the contiguous positions [w*len, (w+1)*len): it counts its left keys,
   // the warps' counts are scanned, then each warp writes its range in order
-  // with ballots (no block barrier inside the loop).
+  // with ballots (no block barrier inside the loop), kUnroll batches of 32
+  // positions loaded at a time.
   constexpr int kWarps = kSplitThreads / 32;
   const int lane = tid & 31, w = tid >> 5;
-  const int len = (nd.n + kWarps - 1) / kWarps;
-  const int lo = min(nd.n, w * len), hi = min(nd.n, lo + len);
+  const int len = (n + kWarps - 1) / kWarps;
+  const int lo = min(n, w * len), hi = min(n, lo + len);
   uint32_t nleft = 0;
-  for (int b = lo; b < hi; b += 32) {
-    const int i = b + lane;
-    nleft += __popc(__ballot_sync(0xffffffffu, i < hi && kk[i] <= T));
+  for (int b = lo; b < hi; b += 32 * kUnroll) {
+    bool left[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = b + 32 * u + lane;
+      left[u] = i < hi && kk[i] <= T;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) nleft += __popc(__ballot_sync(0xffffffffu, left[u]));
   }
   __shared__ uint32_t wleft[kWarps];
   if (lane == 0) wleft[w] = nleft;
@@ -805,16 +834,129 @@ __global__ void __launch_bounds__(kSplitThreads)
   for (int v = 0; v < w; ++v) before_left += wleft[v];
   uint32_t run_left = before_left, run_right = static_cast<uint32_t>(lo) - before_left;
   const unsigned lt = (1u << lane) - 1u;
-  for (int b = lo; b < hi; b += 32) {
+  for (int b = lo; b < hi; b += 32 * kUnroll) {
+    bool left[kUnroll];
+    int32_t val[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = b + 32 * u + lane;
+      left[u] = i < hi && kk[i] <= T;
+      val[u] = i < hi ? in[i] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = b + 32 * u + lane;
+      const bool valid = i < hi;
+      const unsigned ml = __ballot_sync(0xffffffffu, left[u]);
+      const unsigned mr = __ballot_sync(0xffffffffu, valid && !left[u]);
+      if (valid) {
+        const int dst = left[u] ? static_cast<int>(run_left + __popc(ml & lt))
+                                : nl + static_cast<int>(run_right + __popc(mr & lt));
+        if (dst < n && (left[u] ? dst < nl : dst >= nl))
+          out[dst] = val[u];
+        else
+          atomicOr(status, DEV_BOUNDS);
+      }
+      run_left += __popc(ml);
+      run_right += __popc(mr);
+    }
+  }
+}
+
+// One warp per node of at most kSmallNode rows (and per new leaf, which it
+// copies).  The node's keys go to shared memory once; the digit histogram is
+// per warp; a lane scans 8 consecutive bins.
+__global__ void __launch_bounds__(32 * kSmallWarps)
+    pddp_split_small_kernel(const uint64_t* __restrict__ keys, const int32_t* __restrict__ perm_in,
+                            int32_t* __restrict__ perm_out, int N, int C, int depth, int slots,
+                            unsigned* status) {
+  __shared__ uint64_t skeys[kSmallWarps][kSmallNode];
+  __shared__ uint32_t shist[kSmallWarps][256];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int slot = blockIdx.x * kSmallWarps + w, bh = blockIdx.y;
+  if (slot >= slots) return;  // whole warp
+  bool stale = false;
+  const Node nd = node_at(N, C, depth, slot, &stale);
+  if (nd.n == 0 || stale || nd.n > kSmallNode) return;
+  const int32_t* in = perm_in + (size_t)bh * N + nd.start;
+  int32_t* out = perm_out + (size_t)bh * N + nd.start;
+  const int n = nd.n, g = (n + C - 1) / C;
+  if (g <= 1) {  // a leaf appearing at this depth
+    for (int i = lane; i < n; i += 32) out[i] = in[i];
+    return;
+  }
+  const int nl = C * (g / 2);
+  const uint64_t* kk = keys + (size_t)bh * N + nd.start;
+  uint64_t* sk = skeys[w];
+  uint32_t* h = shist[w];
+  for (int i = lane; i < n; i += 32) sk[i] = kk[i];
+  __syncwarp();
+  uint64_t prefix = 0, mask = 0, T = ~0ull;
+  uint32_t remaining = static_cast<uint32_t>(nl);
+  for (int shift = 56; shift >= 0; shift -= 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[lane * 8 + e] = 0;
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
+      const uint64_t k = sk[i];
+      if ((k & mask) == prefix) atomicAdd(&h[(k >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    uint32_t c[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = h[lane * 8 + e];
+      tot += c[e];
+    }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    uint32_t below = incl - tot;
+    int dsel = -1;
+    uint32_t bsel = 0, csel = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (below < remaining && remaining <= below + c[e]) {
+        dsel = lane * 8 + e;
+        bsel = below;
+        csel = c[e];
+      }
+      below += c[e];
+    }
+    const unsigned found = __ballot_sync(0xffffffffu, dsel >= 0);
+    if (found == 0u) {  // cannot happen with distinct keys
+      if (lane == 0) atomicOr(status, DEV_BOUNDS);
+      return;
+    }
+    const int src = __ffs(found) - 1;
+    dsel = __shfl_sync(0xffffffffu, dsel, src);
+    bsel = __shfl_sync(0xffffffffu, bsel, src);
+    csel = __shfl_sync(0xffffffffu, csel, src);
+    prefix |= static_cast<uint64_t>(dsel) << shift;
+    mask |= 255ull << shift;
+    remaining -= bsel;
+    if (remaining == csel) {
+      T = prefix | ~mask;
+      break;
+    }
+    if (shift == 0) T = prefix;
+    __syncwarp();  // every lane has read h before the next pass clears it
+  }
+  uint32_t run_left = 0, run_right = 0;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b = 0; b < n; b += 32) {
     const int i = b + lane;
-    const bool valid = i < hi;
-    const bool left = valid && kk[i] <= T;
+    const bool valid = i < n;
+    const bool left = valid && sk[i] <= T;
     const unsigned ml = __ballot_sync(0xffffffffu, left);
     const unsigned mr = __ballot_sync(0xffffffffu, valid && !left);
     if (valid) {
       const int dst = left ? static_cast<int>(run_left + __popc(ml & lt))
                            : nl + static_cast<int>(run_right + __popc(mr & lt));
-      if (dst < nd.n && (left ? dst < nl : dst >= nl))
+      if (dst < n && (left ? dst < nl : dst >= nl))
         out[dst] = in[i];
       else
         atomicOr(status, DEV_BOUNDS);
@@ -901,8 +1043,13 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
                              proj_smem_bytes<D>(), stream>>>(q, pa, N, C, d, slots, nodevec, keys,
                                                              layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
-                                                                     status);
+    if (max_node_rows(N, C, d) > kSmallNode) {
+      pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
+                                                                       status);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    pddp_split_small_kernel<<<dim3((slots + kSmallWarps - 1) / kSmallWarps, BH),
+                              32 * kSmallWarps, 0, stream>>>(keys, pa, pb, N, C, d, slots, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     int32_t* t = pa;
     pa = pb;
