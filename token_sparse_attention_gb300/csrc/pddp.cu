@@ -21,7 +21,7 @@
 //                  gathered in position order with 16-byte cp.async into a
 //                  swizzled two-stage ring; X^T X on tcgen05 (A = X^T, B = X,
 //                  both MN-major views of the same tile), fp32 in TMEM; the
-//                  column sums on the CUDA cores (16-byte shared loads)
+//                  column sums by one more MMA against a block of ones
 //   pddp_reduce    (nodes of many chunks) sum the chunk partials in chunk order
 //   pddp_power     per (head, node): (sum a few chunk partials in chunk order)
 //                  Cov = X^T X - s s^T / n, then `iters` steps v <- Cov v/|Cov v|
@@ -39,8 +39,9 @@ namespace mcs {
 namespace {
 
 constexpr int kChunkRows = 1024;  // rows per moments CTA (8 tiles of 128)
-constexpr int kMomProducers = 4;  // cp.async producer warps of the moments kernel
-constexpr int kMomMmaWarp = 4 + kMomProducers;
+constexpr int kMomProducers = 8;  // cp.async producer warps of the moments kernel (0-7)
+constexpr int kMomStages = 3;     // ring stages of the moments kernel (two CTAs per SM)
+constexpr int kMomMmaWarp = kMomProducers;
 constexpr int kMomThreads = 32 * (kMomMmaWarp + 1);
 
 struct Node {
@@ -138,11 +139,13 @@ template <int D>
 struct MomLayout {
   // Each stage: two 16 KB sub-tiles [128 rows x 128 B].  For D = 128 they
   // hold columns 0-63 and 64-127; for D = 64 the second one stays zero so
-  // the M = 128 MMA (A = X^T, M = feature) sees zero rows 64-127.
+  // the M = 128 MMA (A = X^T, M = feature) sees zero rows 64-127.  After the
+  // barriers: a 16 x 16 block of bf16 ones, the B operand of the column sums.
   static constexpr int kSubBytes = 128 * 128;
   static constexpr int kStage = 2 * kSubBytes;
-  static constexpr int kBars = 2 * kStage;
-  static constexpr int kUsed = kBars + 128 + 1024;
+  static constexpr int kBars = kMomStages * kStage;
+  static constexpr int kOnes = kBars + 128;
+  static constexpr int kUsed = kOnes + 512 + 1024;
   static constexpr int kSmem = kUsed;
 };
 
@@ -152,8 +155,14 @@ __device__ __forceinline__ int mom_swz(int r, int seg) {
   return (seg >> 3) * (128 * 128) + r * 128 + (((seg & 7) ^ (r & 7)) << 4);
 }
 
+// Per (head, node, chunk): X^T X of the chunk's rows into TMEM columns 0-127
+// and the column sums, X^T 1, into columns 128-143 (one more N = 16 MMA per
+// K step against a block of ones), so that a stage is free again as soon as
+// its MMAs complete.  Warps 0-7 copy rows; warp 8 issues the MMAs; warps 0-3
+// then write the chunk's partial (X^T X, then the column sums).  Two CTAs per
+// SM (256 TMEM columns each).
 template <int D>
-__global__ void __launch_bounds__(kMomThreads, 3)
+__global__ void __launch_bounds__(kMomThreads, 2)
     pddp_moments_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
                         int N, int C, int depth, int slots, int max_chunks, float* partials,
                         unsigned* status, int layout, int H, int head0) {
@@ -162,11 +171,10 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint64_t* full = bars + 0;   // [2] rows landed (every producer thread)
-  uint64_t* ready = bars + 2;  // [2] column sums taken (4 warp arrivals)
-  uint64_t* empty = bars + 4;  // [2] MMA done with the stage
-  uint64_t* done = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  uint64_t* full = bars + 0;            // [kMomStages] rows landed (every producer thread)
+  uint64_t* empty = bars + kMomStages;  // [kMomStages] MMA done with the stage
+  uint64_t* done = bars + 2 * kMomStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMomStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int chunk = blockIdx.x, slot = blockIdx.y, bh = blockIdx.z;
@@ -177,25 +185,30 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   const int warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kMomStages; ++s) {
       mbar_init(full + s, kMomProducers * 32);
-      mbar_init(ready + s, 4);
       mbar_init(empty + s, 1);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (D == 64 && warp < 4) {
-    // zero the second sub-tile of both stages
-    for (int i = threadIdx.x; i < 2 * (128 * 128) / 16; i += 128) {
-      const int st = i / ((128 * 128) / 16), o = i % ((128 * 128) / 16);
-      reinterpret_cast<uint4*>(smem + st * L::kStage + L::kSubBytes)[o] = make_uint4(0, 0, 0, 0);
+  if (warp < 4) {
+    // the ones block (bf16 1.0 = 0x3F80), and for D = 64 zeros in the second
+    // sub-tile of both stages
+    if (threadIdx.x < 32)
+      reinterpret_cast<uint4*>(smem + L::kOnes)[threadIdx.x] =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    if (D == 64) {
+      for (int i = threadIdx.x; i < kMomStages * (128 * 128) / 16; i += 128) {
+        const int st = i / ((128 * 128) / 16), o = i % ((128 * 128) / 16);
+        reinterpret_cast<uint4*>(smem + st * L::kStage + L::kSubBytes)[o] = make_uint4(0, 0, 0, 0);
+      }
     }
     fence_proxy_async_smem();
   }
   if (warp == kMomMmaWarp) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -205,35 +218,39 @@ __global__ void __launch_bounds__(kMomThreads, 3)
   const int32_t* pos = perm + (size_t)bh * N + nd.start + chunk * kChunkRows;
   const RowMap rm = row_map(layout, H, N, head0 + bh);  // rows of q in either layout
 
-  if (warp >= 4 && warp < kMomMmaWarp) {
+  bool ok = true;
+  if (warp < kMomProducers) {
     // ------------------------------------------------------------ producers
-    // Producer warp pw copies rows 32 pw .. 32 pw + 31 of each tile with
+    // Producer warp pw copies rows 16 pw .. 16 pw + 15 of each tile with
     // 16-byte cp.async (kRPI whole rows per warp instruction, written in the
-    // swizzled layout); lane l reads the token of row 32 pw + l once and
-    // broadcasts it.  Rows past the node end are zero-filled.
-    constexpr int kSegs = D * 2 / 16;  // 16-byte segments per row
-    constexpr int kRPI = 32 / kSegs;   // rows per warp instruction
-    const int pw = warp - 4;
+    // swizzled layout); lane l < 16 reads the token of row 16 pw + l (the
+    // next tile's one tile ahead) and broadcasts it.  Rows past the node end
+    // are zero-filled.
+    constexpr int kRows = 128 / kMomProducers;  // rows of a tile per warp
+    constexpr int kSegs = D * 2 / 16;           // 16-byte segments per row
+    constexpr int kRPI = 32 / kSegs;            // rows per warp instruction
+    static_assert(kRows % kRPI == 0, "whole rows per warp instruction");
+    const int pw = warp;
     const int sub = lane / kSegs, seg = lane % kSegs;
+    const int myr = pw * kRows + (lane % kRows);
     bool bad = false;
-    // the token of the lane's row of tile j + 1 is loaded while tile j is copied
-    int tnext = pw * 32 + lane < rows ? __ldg(pos + pw * 32 + lane) : -1;
+    int tnext = myr < rows ? __ldg(pos + myr) : -1;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      const int rr = j * 128 + pw * 32 + lane;
+      const int st = j % kMomStages;
+      const int rr = j * 128 + myr;
       int t = tnext;
       if (j + 1 < ntiles) tnext = rr + 128 < rows ? __ldg(pos + rr + 128) : -1;
       if (t >= N || (rr < rows && t < 0)) { bad = true; t = -1; }
       const int myrow = t < 0 ? -1 : rm.rbase + t * rm.rstride;
-      if (j >= 2) {
-        bool ok = mbar_wait(empty + st, ((j >> 1) - 1) & 1, abort_flag, status);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      if (j >= kMomStages) {  // the stage's previous tile, j - kMomStages, is multiplied
+        bool w = mbar_wait(empty + st, (j / kMomStages - 1) & 1, abort_flag, status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       }
       uint8_t* stage = smem + st * L::kStage;
 #pragma unroll
-      for (int i = 0; i < 32 / kRPI; ++i) {
+      for (int i = 0; i < kRows / kRPI; ++i) {
         const int row = __shfl_sync(0xffffffffu, myrow, i * kRPI + sub);
-        const int r = pw * 32 + i * kRPI + sub;
+        const int r = pw * kRows + i * kRPI + sub;
         cp_async16_zfill(stage + mom_swz(r, seg),
                          q + (size_t)(row < 0 ? 0 : row) * D + seg * 8, row >= 0);
       }
@@ -241,15 +258,17 @@ __global__ void __launch_bounds__(kMomThreads, 3)
     }
     if (bad) atomicOr(status, DEV_BOUNDS);
     asm volatile("cp.async.wait_all;" ::: "memory");  // every copy lands before exit
-  } else if (warp == kMomMmaWarp) {
+  } else {
     // ------------------------------------------------------------ MMA
     // whole warp in the loop, one elected lane issues (a lane-0-only branch
     // issues MMAs much more slowly)
     constexpr uint32_t idesc = idesc_bf16(128, D, true, true);
+    constexpr uint32_t idesc_sum = idesc_bf16(128, 16, true, false);
+    const uint64_t ones = sdesc_none(smem_u32(smem + L::kOnes), 128, 256);
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      const bool ok = mbar_wait(ready + st, (j >> 1) & 1, abort_flag, status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      const int st = j % kMomStages;
+      const bool w = mbar_wait(full + st, (j / kMomStages) & 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       fence_proxy_async_smem();  // rows written by cp.async, read by the MMA
       tc_fence_after();
       const uint32_t base = smem_u32(smem + st * L::kStage);
@@ -257,95 +276,60 @@ __global__ void __launch_bounds__(kMomThreads, 3)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t d = sdesc_sw128(base + kk * 16 * 128, L::kSubBytes, 1024);
-          umma_ss(tmem, d, d, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          umma_ss(tmem, d, d, idesc, acc);
+          umma_ss(tmem + 128, d, ones, idesc_sum, acc);
         }
         umma_commit(empty + st);
       }
-    }
-    if (elect_one()) umma_commit(done);
-    __syncwarp();
-    const long long t0 = clock64();
-    while (!mbar_try_wait(done, 0))
-      if (clock64() - t0 > kWaitLimitCycles) break;
-  } else {
-    // ------------------------------------------------------------ column sums, epilogue
-    // Thread t sums the 16-byte chunk cc = t % kCC (8 columns) over the rows
-    // of row group t / kCC of every tile (rows past the node end are zero);
-    // the row groups' partial sums are added at the end.
-    constexpr int kCC = D / 8;        // 16-byte chunks per row
-    constexpr int kRG = 128 / kCC;    // row groups
-    constexpr int kRPG = 128 / kRG;   // rows per group
-    const int t = threadIdx.x;  // 0..127
-    const int cc = t % kCC, rgp = t / kCC;
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      bool w = mbar_wait(full + st, (j >> 1) & 1, abort_flag, status);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      const uint8_t* stage = smem + st * L::kStage;
-#pragma unroll 4
-      for (int i = 0; i < kRPG; ++i) {
-        const int r = rgp * kRPG + i;
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + mom_swz(r, cc));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h[e]);
-          acc[2 * e] += f.x;
-          acc[2 * e + 1] += f.y;
-        }
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(ready + st);
-      // the producers may overwrite this stage only after the MMA's commit,
-      // which follows every compute warp's arrival
     }
-    // partial column sums of the row groups -> shared memory (the first
-    // stage: every copy into it has landed and the MMA reads it no more
-    // once `done` completes), summed below in row-group order
-    float colsum = 0.f;
+    if (elect_one()) umma_commit(done);  // after every MMA issued (or none)
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ epilogue
+  // warps 0-3: TMEM lane t = feature row t
+  if (warp < 4) {
+    ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      bool w = mbar_wait(done, 0, abort_flag, status);
+      const bool w = mbar_wait(done, 0, abort_flag, status);
       ok = __all_sync(0xffffffffu, w);
-    }
-    float* red = reinterpret_cast<float*>(smem);
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3: stage 0 free of readers
-    if (ok) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) red[rgp * D + cc * 8 + e] = acc[e];
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ok && t < D) {
-      for (int g = 0; g < kRG; ++g) colsum += red[g * D + t];
     }
     if (ok) {
       tc_fence_after();
+      const int t = threadIdx.x;  // 0..127
       float* out = partials + ((size_t)(bh * slots + slot) * max_chunks + chunk) * (D * D + D);
       const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+      // thread t holds row t of X^T X; the matrix is symmetric, so it stores
+      // its 32 columns c*32+i as column t of rows c*32+i: one coalesced
+      // 128-byte row segment per warp and store
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + c * 32, v);
         tmem_ld_wait();
         if (t < D) {
-          float4* o4 = reinterpret_cast<float4*>(out + t * D + c * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          for (int i = 0; i < 32; ++i) out[(c * 32 + i) * D + t] = __uint_as_float(v[i]);
         }
       }
-      if (t < D) out[D * D + t] = colsum;
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + 128, v);
+      tmem_ld_wait();
+      if (t < D) out[D * D + t] = __uint_as_float(v[0]);
     }
+  } else if (warp == kMomMmaWarp) {
+    // drain: every MMA this CTA issued completes before TMEM is freed
+    const long long t0 = clock64();
+    while (!mbar_try_wait(done, 0))
+      if (clock64() - t0 > kWaitLimitCycles) break;
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMomMmaWarp) tmem_dealloc(tmem, 128);
+  if (warp == kMomMmaWarp) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------- power iteration
@@ -608,11 +592,12 @@ constexpr int proj_smem_bytes() { return (kProjThreads / 32) * 32 * D * 2; }
 // partial (x - mu).v for all 32 rows with the node's mean and direction in
 // registers, and a butterfly transpose reduction leaves row l's projection
 // in lane l.
-template <int D>
+template <int D, int C>
 __global__ void __launch_bounds__(kProjThreads)
     pddp_project_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
-                        int N, int C, int depth, int slots, const float* __restrict__ nodevec,
+                        int N, int depth, int slots, const float* __restrict__ nodevec,
                         uint64_t* __restrict__ keys, int layout, int H, int head0) {
+  // C is a template argument: the node walk of every position divides by it
   constexpr int E = D / 32;          // elements of a row per lane: 4 (D = 128) or 2 (D = 64)
   constexpr int kSegs = D * 2 / 16;  // 16-byte chunks per row
   static_assert(E == 2 || E == 4, "D must be 64 or 128");
@@ -1020,7 +1005,8 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
                            msmem);
   if (e != cudaSuccess) return e;
   const int psmem = 0;  // the power kernel's shared memory is static
-  e = cudaFuncSetAttribute(pddp_project_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto project = C == 64 ? pddp_project_kernel<D, 64> : pddp_project_kernel<D, 128>;
+  e = cudaFuncSetAttribute(project, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            proj_smem_bytes<D>());
   if (e != cudaSuccess) return e;
 
@@ -1039,9 +1025,8 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
     pddp_power_kernel<D><<<dim3(slots, BH), kPowThreads, psmem, stream>>>(partials, N, C, d, slots,
                                                                           chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    pddp_project_kernel<D><<<dim3((N + kProjThreads - 1) / kProjThreads, BH), kProjThreads,
-                             proj_smem_bytes<D>(), stream>>>(q, pa, N, C, d, slots, nodevec, keys,
-                                                             layout, H, head0);
+    project<<<dim3((N + kProjThreads - 1) / kProjThreads, BH), kProjThreads, proj_smem_bytes<D>(),
+              stream>>>(q, pa, N, d, slots, nodevec, keys, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (max_node_rows(N, C, d) > kSmallNode) {
       pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
