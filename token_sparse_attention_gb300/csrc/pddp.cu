@@ -588,19 +588,19 @@ constexpr int proj_smem_bytes() { return (kProjThreads / 32) * 32 * D * 2; }
 
 // One warp per 32 consecutive positions of a head.  The warp copies its 32
 // rows into shared memory with 16-byte cp.async (all loads in flight at
-// once), then lane l takes elements [l*E, (l+1)*E) of every row, forms its
-// partial (x - mu).v for all 32 rows with the node's mean and direction in
-// registers, and a butterfly transpose reduction leaves row l's projection
-// in lane l.
+// once); each half-warp then takes every other row, its lane hl the elements
+// [hl*D/16, (hl+1)*D/16) of each, forms the partial (x - mu).v of its 16
+// rows with the node's mean and direction in registers, and a butterfly
+// transpose reduction over the half-warp leaves one row's projection per
+// lane.
 template <int D, int C>
 __global__ void __launch_bounds__(kProjThreads)
     pddp_project_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
                         int N, int depth, int slots, const float* __restrict__ nodevec,
                         uint64_t* __restrict__ keys, int layout, int H, int head0) {
   // C is a template argument: the node walk of every position divides by it
-  constexpr int E = D / 32;          // elements of a row per lane: 4 (D = 128) or 2 (D = 64)
   constexpr int kSegs = D * 2 / 16;  // 16-byte chunks per row
-  static_assert(E == 2 || E == 4, "D must be 64 or 128");
+  static_assert(D == 64 || D == 128, "D must be 64 or 128");
   extern __shared__ __align__(16) uint8_t proj_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int p0 = (blockIdx.x * (kProjThreads / 32) + wid) * 32;
@@ -643,42 +643,48 @@ __global__ void __launch_bounds__(kProjThreads)
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncwarp();
-  float acc[32];
+  // half-warp hp takes rows 2i + hp (i < 16); its lane hl the elements
+  // [hl*E2, hl*E2 + E2) of each (one 16-byte (D = 128) or 8-byte shared load)
+  constexpr int E2 = D / 16;
+  const int hl = lane & 15, hp = lane >> 4;
+  float acc[16];
   int cached = -1;
-  float vs[E], ms[E];
+  float vs[E2], ms[E2];
 #pragma unroll
-  for (int e = 0; e < E; ++e) vs[e] = ms[e] = 0.f;
+  for (int e = 0; e < E2; ++e) vs[e] = ms[e] = 0.f;
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
+  for (int i = 0; i < 16; ++i) {
+    const int r = 2 * i + hp;
     const int sr = __shfl_sync(0xffffffffu, slot, r);
-    acc[r] = 0.f;
-    if (sr >= 0) {  // the same for the whole warp
+    acc[i] = 0.f;
+    if (sr >= 0) {
       if (sr != cached) {
-        const float* vec = nodevec + (size_t)(bh * slots + sr) * 2 * D + lane * E;
+        const float* vec = nodevec + (size_t)(bh * slots + sr) * 2 * D + hl * E2;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
+        for (int e = 0; e < E2; ++e) {
           vs[e] = __ldg(vec + e);
           ms[e] = __ldg(vec + D + e);
         }
         cached = sr;
       }
       const __nv_bfloat162* x =
-          reinterpret_cast<const __nv_bfloat162*>(buf + r * D * 2 + lane * E * 2);
+          reinterpret_cast<const __nv_bfloat162*>(buf + r * D * 2 + hl * E2 * 2);
       float t = 0.f;
 #pragma unroll
-      for (int h = 0; h < E / 2; ++h) {
+      for (int h = 0; h < E2 / 2; ++h) {
         const float2 f = __bfloat1622float2(x[h]);
         t = fmaf(f.x - ms[2 * h], vs[2 * h], t);
         t = fmaf(f.y - ms[2 * h + 1], vs[2 * h + 1], t);
       }
-      acc[r] = t;
+      acc[i] = t;
     }
   }
-  // transpose reduction: after the step of width w, a lane keeps the w rows
-  // whose index has its lane's bit w, summed with its partner's
+  // transpose reduction over the half-warp: after the step of width w, a lane
+  // keeps the w rows whose index has its lane's bit w, summed with its
+  // partner's; lane hl ends with row index i = hl, i.e. row 2 hl + hp
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool upper = (hl & w) != 0;
 #pragma unroll
     for (int i = 0; i < w; ++i) {
       const float send = upper ? acc[i] : acc[i + w];
@@ -686,10 +692,13 @@ __global__ void __launch_bounds__(kProjThreads)
       acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
     }
   }
-  if (slot >= 0) {
+  const int r = 2 * hl + hp;
+  const int s_r = __shfl_sync(0xffffffffu, slot, r);
+  const int tok_r = __shfl_sync(0xffffffffu, token, r);
+  if (s_r >= 0) {
     uint32_t u = __float_as_uint(acc[0]);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // unsigned order == float order
-    keys[(size_t)bh * N + p] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(token);
+    keys[(size_t)bh * N + p0 + r] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(tok_r);
   }
 }
 
