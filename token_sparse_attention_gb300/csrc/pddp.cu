@@ -765,6 +765,7 @@ __global__ void __launch_bounds__(kSplitThreads)
   uint64_t T = ~0ull;
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += kSplitThreads) hist[b] = 0;
+    if (tid == 0) sel_digit = 256;  // none yet
     __syncthreads();
     for (int i0 = tid; i0 < n; i0 += kUnroll * kSplitThreads) {
       uint64_t k[kUnroll];
@@ -790,6 +791,10 @@ __global__ void __launch_bounds__(kSplitThreads)
       }
     }
     __syncthreads();
+    if (sel_digit >= 256u) {  // cannot happen with distinct keys (block-uniform)
+      if (tid == 0) atomicOr(status, DEV_BOUNDS);
+      return;
+    }
     const uint32_t cnt = hist[sel_digit];
     prefix |= static_cast<uint64_t>(sel_digit) << shift;
     mask |= 255ull << shift;
