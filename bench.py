@@ -83,6 +83,27 @@ def depths_of(G: int) -> int:
     return max(0, math.ceil(math.log2(G))) if G > 1 else 0
 
 
+def pddp_launches(N: int, C: int) -> int:
+    """Kernel launches of one mcs_group call: init and finalize, then per
+    depth moments, power iteration, projection and the warp-per-node split,
+    plus the chunk-partial reduction when a node has >= 4 chunks of 1024 rows
+    and the block-per-node split when a node has > 1024 rows (pddp.cu)."""
+    G = -(-N // C)
+    nodes, count = [N], 2
+    for _ in range(depths_of(G)):
+        mx = max(nodes)
+        count += 4 + (1 if -(-mx // 1024) >= 4 else 0) + (1 if mx > 1024 else 0)
+        nxt = []
+        for n in nodes:
+            g = -(-n // C)
+            if g <= 1:
+                nxt.append(n)
+            else:
+                nxt += [C * (g // 2), n - C * (g // 2)]
+        nodes = nxt
+    return count
+
+
 def pddp_bytes(BH: int, N: int, D: int, G: int) -> float:
     """Algorithmic HBM bytes of the PDDP grouping: per depth, every head's
     rows read twice (moments and projection, bf16) plus the index traffic
@@ -487,13 +508,12 @@ def run_gpu(args, w, K, rank, world, dist):
                  / float(peaks.get("hbm_gbs", 6800.0)),
                  "peak": "hbm_gbs (" + peak_kind + ")"},
     }
-    depths = max(0, math.ceil(math.log2(G))) if G > 1 else 0
     # mcs_select passes the heads through the workspace in chunks; each chunk
     # is one group-mass and one top-K launch
     rup = lambda x: -(-x // 256) * 256  # noqa: E731
     chunk = max(1, min(BH, ws_bytes // (rup(G * w.N * 4) + rup(G * 1088 * 4))))
     n_chunks = -(-BH // chunk)
-    launches = (2 + 4 * depths) + 1 + 2 * n_chunks + 1 + R
+    launches = pddp_launches(w.N, w.C) + 1 + 2 * n_chunks + 1 + R
     cores = len(os.sched_getaffinity(0))
     cpu = None
     if not args.no_cpu_baseline:

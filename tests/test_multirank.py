@@ -97,6 +97,16 @@ def test_head_slices_are_views_and_params_match():
         shard.slice_params(p, 4, 7)
 
 
+def test_pddp_launch_count_matches_the_launch_list():
+    # the large video workload's grouping launched 54 kernels in the ncu launch
+    # list of the bench step (10 depths x 4, reduce at depths 0-4, block split
+    # at depths 0-6, init, finalize); the 3D workload's nodes of 1024 rows at
+    # depth 6 take the warp split only
+    assert bench.pddp_launches(75600, 128) == 54
+    assert bench.pddp_launches(65536, 64) == 2 + 40 + 5 + 6
+    assert bench.pddp_launches(100, 128) == 2  # one group: no depth
+
+
 def test_bench_rank_heads_weak_and_strong():
     w = synth.workload("large")
     wg, h0, h1 = bench.rank_heads(w, 0, 1, "weak")
