@@ -178,6 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     kv_len[1] = min(max(kv_len[1], 1), a.cap);
   }
   const int nkv = (max(kv_len[0], kv_len[1]) + BN - 1) / BN;
+  // Unpaired C = 64 groups fill half a 128-row tile: unit a's rows go to tile
+  // rows 0-63 (TMEM lanes read by warps 0-1), unit b's to rows 64-127 (warps
+  // 6-7), so that each scheduler runs one busy softmax warp instead of two
+  // (a warp may only read its own quarter of the TMEM lanes); the warps of
+  // the empty rows keep only the hand-off protocol.
+  const int qoff_b = (kSparseMode && !kPairs && a.C <= BM / 2) ? BM / 2 : 0;
+  auto qoff = [&](int x) { return x == 1 ? qoff_b : 0; };
   // Ring items, numbered in the order the MMA warp consumes them (item i
   // goes to stage i % NS).  Dense: K(j) = 2j, V(j) = 2j+1, each shared by
   // both units.  Sparse: K_a(0) = 0, K_b(0) = 1, then per step j
@@ -305,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = tid + kPT * k;
           if (c < kChunks) {
             const int r = c / kSegs, sg = c % kSegs;
-            int tok = (r < qrows && (x == 0 || has_b)) ? __ldg(perm_g + r) : -1;
+            const int gr = r - qoff(x);  // the group's row in this tile row
+            int tok = (gr >= 0 && gr < qrows && (x == 0 || has_b)) ? __ldg(perm_g + gr) : -1;
             if (tok >= a.N) { bad = true; tok = -1; }
             const __nv_bfloat16* src =
                 a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + sg * 8;
@@ -510,12 +518,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_f32 = 0.f, l_b16 = 0.f;
     bool ok = true;
+    // this warp's 32 rows hold none of the unit's queries (warp-uniform)
+    const bool idle = kSparseMode && !kPairs &&
+                      ((warp & 3) * 32 + 32 <= qoff(x) || (warp & 3) * 32 >= qoff(x) + a.C);
     for (int j = 0; j < nkv; ++j) {
       if (!wait_batch(j == 0 ? 0 : 2 * j + x - 1)) {  // S_x(j) written
         ok = false;
         break;
       }
       tc_fence_after();
+      if (idle) {  // P of these rows is never read back: hand S straight on
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + x);
+        continue;
+      }
       const int valid = kv_mine - j * BN;
       float s[64];
       uint32_t* su = reinterpret_cast<uint32_t*>(s);
@@ -614,8 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // may not exist when G is odd)
         const int g0 = kPairs ? 2 * unit : unit;
         const int qrows = kPairs ? (g0 + 1 < a.G ? 2 : 1) * a.C : a.C;
-        token = (row < qrows && (x == 0 || has_b))
-                    ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g0) * a.C + row)
+        const int gr = row - qoff(x);
+        token = (!idle && gr >= 0 && gr < qrows && (x == 0 || has_b))
+                    ? __ldg(a.perm + (static_cast<size_t>(bh) * a.G + g0) * a.C + gr)
                     : -1;
         if (token >= a.N) token = -1;
       }
