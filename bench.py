@@ -50,11 +50,11 @@ METRIC = "sparse-attn effective TFLOP/s & speedup vs own dense attn at N=75600, 
 # while the source is unchanged).
 TRAFFIC = {
     # ncu dram bytes (read + write) of the sparse reuse launch, captured on the
-    # 4-head large workload (mean of two launches of `bench.py --heads 4
-    # --steps 1 --warmup 1 --no-e2e --no-cpu-baseline --no-workloads`), times
-    # 10 for the 40-head launch: heads are independent and the grid scales
-    # with them
-    "attn.cu": {"sha": "6dbdbda25108", "bytes_per_launch": 7252938240},
+    # 4-head large workload (the timed step's first reuse launch of `bench.py
+    # --heads 4 --steps 1 --warmup 1 --no-e2e --no-cpu-baseline
+    # --no-workloads`), times 10 for the 40-head launch: heads are independent
+    # and the grid scales with them
+    "attn.cu": {"sha": "34c2b542de82", "bytes_per_launch": 7315973120},
 }
 
 
