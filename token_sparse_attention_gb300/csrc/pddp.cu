@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kPowThreads, 2)
 
 // ---------------------------------------------------------------- projection
 
-constexpr int kProjThreads = 256;
+constexpr int kProjThreads = 32;  // one warp per CTA: a finished warp's slot is refilled at once
 
 template <int D>
 constexpr int proj_smem_bytes() { return (kProjThreads / 32) * 32 * D * 2; }
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(kProjThreads)
 
 constexpr int kSplitThreads = 512;
 constexpr int kSmallNode = 1024;
-constexpr int kSmallWarps = 4;
+constexpr int kSmallWarps = 1;  // nodes (warps) per CTA
 constexpr int kUnroll = 4;
 
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, uint32_t* total) {
