@@ -713,10 +713,10 @@ __global__ void __launch_bounds__(kProjThreads)
 // and no block barrier.  A leaf is copied to the output buffer once, at the
 // depth where it appears; from then on both buffers hold its final positions.
 
-constexpr int kSplitThreads = 512;
+constexpr int kSplitThreads = 1024;
 constexpr int kSmallNode = 1024;
 constexpr int kSmallWarps = 1;  // nodes (warps) per CTA
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
