@@ -713,14 +713,13 @@ __global__ void __launch_bounds__(kProjThreads)
 // and no block barrier.  A leaf is copied to the output buffer once, at the
 // depth where it appears; from then on both buffers hold its final positions.
 
-constexpr int kSplitThreads = 1024;
 constexpr int kSmallNode = 1024;
+constexpr int kSplitWide = 16384;  // nodes above this many rows split with 1024 threads
 constexpr int kSmallWarps = 1;  // nodes (warps) per CTA
-constexpr int kUnroll = 8;
 
+template <int kWarps>
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kWarps = kSplitThreads / 32;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
@@ -744,6 +743,10 @@ __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, 
   return v + before;
 }
 
+// Nodes of more than kSmallNode rows: one CTA of kSplitThreads threads each,
+// kUnroll keys per thread in flight.  1024 threads for the top depths (a few
+// nodes of tens of thousands of rows), 256 below (more nodes, more CTAs per SM).
+template <int kSplitThreads, int kUnroll>
 __global__ void __launch_bounds__(kSplitThreads)
     pddp_split_kernel(const uint64_t* __restrict__ keys, const int32_t* __restrict__ perm_in,
                       int32_t* __restrict__ perm_out, int N, int C, int depth, unsigned* status) {
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(kSplitThreads)
     __syncthreads();
     uint32_t mine = tid < 256 ? hist[tid] : 0u;
     uint32_t total;
-    const uint32_t incl = block_scan_incl(mine, wsum, &total);
+    const uint32_t incl = block_scan_incl<kSplitThreads / 32>(mine, wsum, &total);
     if (tid < 256) {
       const uint32_t below = incl - mine;
       if (below < remaining && remaining <= incl) {
@@ -1043,7 +1046,11 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
               stream>>>(q, pa, N, d, slots, nodevec, keys, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (max_node_rows(N, C, d) > kSmallNode) {
-      pddp_split_kernel<<<dim3(slots, BH), kSplitThreads, 0, stream>>>(keys, pa, pb, N, C, d,
+      if (max_node_rows(N, C, d) > kSplitWide)
+        pddp_split_kernel<1024, 8><<<dim3(slots, BH), 1024, 0, stream>>>(keys, pa, pb, N, C, d,
+                                                                         status);
+      else
+        pddp_split_kernel<256, 4><<<dim3(slots, BH), 256, 0, stream>>>(keys, pa, pb, N, C, d,
                                                                        status);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
