@@ -98,13 +98,13 @@ def test_head_slices_are_views_and_params_match():
 
 
 def test_pddp_launch_count_matches_the_launch_list():
-    # the large video workload's grouping launched 54 kernels in the ncu launch
-    # list of the bench step (10 depths x 4, reduce at depths 0-4, block split
-    # at depths 0-6, init, finalize); the 3D workload's nodes of 1024 rows at
-    # depth 6 take the warp split only
-    assert bench.pddp_launches(75600, 128) == 54
-    assert bench.pddp_launches(65536, 64) == 2 + 40 + 5 + 6
-    assert bench.pddp_launches(100, 128) == 2  # one group: no depth
+    # the large video workload's grouping launched 55 kernels in the ncu launch
+    # list of one call (10 depths x 4, reduce at depths 0-4, block split at
+    # depths 0-6, init, node table, finalize); the 3D workload's nodes of 1024
+    # rows at depth 6 take the warp split only
+    assert bench.pddp_launches(75600, 128) == 55
+    assert bench.pddp_launches(65536, 64) == 3 + 40 + 5 + 6
+    assert bench.pddp_launches(100, 128) == 2  # one group: no depth, no table
 
 
 def test_bench_rank_heads_weak_and_strong():

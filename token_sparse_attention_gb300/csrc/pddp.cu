@@ -93,7 +93,7 @@ int max_node_rows(int N, int C, int depth) {
 }
 
 struct WsLayout {
-  size_t perm_a, perm_b, keys, partials, nodevec, total;
+  size_t perm_a, perm_b, keys, partials, nodevec, table, total;
   int max_chunks_slots;  // max over depths of slots * chunks per node
   int max_slots;
 };
@@ -122,11 +122,55 @@ WsLayout ws_layout(int BH, int N, int D, int C) {
   off += align256(sizeof(float) * (size_t)BH * mcs * (D * D + D));
   w.nodevec = off;
   off += align256(sizeof(float) * (size_t)BH * ms * 2 * D);
+  w.table = off;  // per depth: the slots of the nodes that split, ascending
+  off += align256(sizeof(int32_t) * (size_t)(depths > 0 ? depths : 1) * ms);
   w.total = off;
   return w;
 }
 
+// Number of nodes that split at `depth` (g > 1); the same for every head.
+int split_count(int N, int C, int depth) {
+  int k = 0;
+  for (int s = 0; s < (1 << depth); ++s) {
+    const Node nd = node_at(N, C, depth, s);
+    if ((nd.n + C - 1) / C > 1) ++k;
+  }
+  return k;
+}
+
 // ---------------------------------------------------------------- init
+
+// Block d lists, ascending, the slots of the nodes that split at depth d, so
+// that the per-node kernels of a depth launch one CTA per such node (the deep
+// levels hold many empty slots and leaves).
+constexpr int kTableThreads = 256;
+
+__global__ void __launch_bounds__(kTableThreads)
+    pddp_table_kernel(int N, int C, int max_slots, int32_t* __restrict__ table) {
+  __shared__ int wcount[kTableThreads / 32];
+  const int d = blockIdx.x, slots = 1 << d;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int run = 0;  // entries written by earlier rounds
+  for (int base = 0; base < slots; base += kTableThreads) {
+    const int s = base + tid;
+    bool split = false;
+    if (s < slots) {
+      const Node nd = node_at(N, C, d, s);
+      split = (nd.n + C - 1) / C > 1;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, split);
+    if (lane == 0) wcount[w] = __popc(m);
+    __syncthreads();
+    int before = run, total = run;
+    for (int v = 0; v < kTableThreads / 32; ++v) {
+      if (v < w) before += wcount[v];
+      total += wcount[v];
+    }
+    if (split) table[(size_t)d * max_slots + before + __popc(m & ((1u << lane) - 1u))] = s;
+    run = total;
+    __syncthreads();  // wcount is rewritten by the next round
+  }
+}
 
 __global__ void pddp_init_kernel(int32_t* perm, int N, int BH) {
   const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -164,8 +208,9 @@ __device__ __forceinline__ int mom_swz(int r, int seg) {
 template <int D>
 __global__ void __launch_bounds__(kMomThreads, 2)
     pddp_moments_kernel(const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ perm,
-                        int N, int C, int depth, int slots, int max_chunks, float* partials,
-                        unsigned* status, int layout, int H, int head0) {
+                        const int32_t* __restrict__ slot_tab, int N, int C, int depth, int slots,
+                        int max_chunks, float* partials, unsigned* status, int layout, int H,
+                        int head0) {
   using L = MomLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -177,7 +222,7 @@ __global__ void __launch_bounds__(kMomThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMomStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int chunk = blockIdx.x, slot = blockIdx.y, bh = blockIdx.z;
+  const int chunk = blockIdx.x, slot = slot_tab[blockIdx.y], bh = blockIdx.z;
   const Node nd = node_at(N, C, depth, slot);
   if ((nd.n + C - 1) / C <= 1 || chunk * kChunkRows >= nd.n) return;  // uniform exit
   const int rows = min(kChunkRows, nd.n - chunk * kChunkRows);
@@ -344,12 +389,12 @@ constexpr int kReduceChunks = 4;
 
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads)
-    pddp_reduce_kernel(float* __restrict__ partials, int N, int C, int depth, int slots,
-                       int max_chunks) {
+    pddp_reduce_kernel(float* __restrict__ partials, const int32_t* __restrict__ slot_tab, int N,
+                       int C, int depth, int slots, int max_chunks) {
   constexpr int DD = D * D + D;
   static_assert(DD % 4 == 0, "partials are float4 vectors");
   const int q4 = blockIdx.x * kReduceThreads + threadIdx.x;
-  const int slot = blockIdx.y, bh = blockIdx.z;
+  const int slot = slot_tab[blockIdx.y], bh = blockIdx.z;
   if (q4 * 4 >= DD) return;
   const Node nd = node_at(N, C, depth, slot);
   const int nchunks = (nd.n + kChunkRows - 1) / kChunkRows;
@@ -390,8 +435,9 @@ constexpr int kPowThreads = 256;
 // pipe, not the FMAs, set the pace of the deep levels.)
 template <int D>
 __global__ void __launch_bounds__(kPowThreads, 2)
-    pddp_power_kernel(const float* __restrict__ partials, int N, int C, int depth, int slots,
-                      int max_chunks, int iters, float* __restrict__ nodevec) {
+    pddp_power_kernel(const float* __restrict__ partials, const int32_t* __restrict__ slot_tab,
+                      int N, int C, int depth, int slots, int max_chunks, int iters,
+                      float* __restrict__ nodevec) {
   constexpr int R = D / 16;  // rows per thread: 8 (D = 128) or 4 (D = 64)
   constexpr int J = D / 64;  // 4-column pieces per thread: 2 or 1
   constexpr int kNormEvery = 8;
@@ -401,7 +447,7 @@ __global__ void __launch_bounds__(kPowThreads, 2)
   __shared__ __align__(16) float vb[2][D];  // the iterate, double-buffered
   __shared__ float red[kPowThreads / 32];
   __shared__ int lead;
-  const int slot = blockIdx.x, bh = blockIdx.y;
+  const int slot = slot_tab[blockIdx.x], bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
   if ((nd.n + C - 1) / C <= 1) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -749,11 +795,12 @@ __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* wsum, 
 template <int kSplitThreads, int kUnroll>
 __global__ void __launch_bounds__(kSplitThreads)
     pddp_split_kernel(const uint64_t* __restrict__ keys, const int32_t* __restrict__ perm_in,
-                      int32_t* __restrict__ perm_out, int N, int C, int depth, unsigned* status) {
+                      int32_t* __restrict__ perm_out, const int32_t* __restrict__ slot_tab, int N,
+                      int C, int depth, unsigned* status) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[32];
   __shared__ uint32_t sel_digit, sel_below;
-  const int slot = blockIdx.x, bh = blockIdx.y;
+  const int slot = slot_tab[blockIdx.x], bh = blockIdx.y;
   const Node nd = node_at(N, C, depth, slot);
   const int g = (nd.n + C - 1) / C;
   if (g <= 1 || nd.n <= kSmallNode) return;  // leaves and small nodes: the warp path
@@ -1009,6 +1056,7 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
   uint64_t* keys = reinterpret_cast<uint64_t*>(base + w.keys);
   float* partials = reinterpret_cast<float*>(base + w.partials);
   float* nodevec = reinterpret_cast<float*>(base + w.nodevec);
+  int32_t* table = reinterpret_cast<int32_t*>(base + w.table);
   const int G = (N + C - 1) / C;
   const int depths = depth_count(N, C);
 
@@ -1016,6 +1064,10 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
   pddp_init_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(pa, N, BH);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (depths > 0) {
+    pddp_table_kernel<<<depths, kTableThreads, 0, stream>>>(N, C, w.max_slots, table);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   const int msmem = MomLayout<D>::kSmem;
   e = cudaFuncSetAttribute(pddp_moments_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1030,28 +1082,30 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
   for (int d = 0; d < depths; ++d) {
     const int slots = 1 << d;
     const int chunks = (max_node_rows(N, C, d) + kChunkRows - 1) / kChunkRows;
-    pddp_moments_kernel<D><<<dim3(chunks, slots, BH), kMomThreads, msmem, stream>>>(
-        q, pa, N, C, d, slots, chunks, partials, status, layout, H, head0);
+    const int nsplit = split_count(N, C, d);  // >= 1 below depth_count
+    const int32_t* tab = table + (size_t)d * w.max_slots;
+    pddp_moments_kernel<D><<<dim3(chunks, nsplit, BH), kMomThreads, msmem, stream>>>(
+        q, pa, tab, N, C, d, slots, chunks, partials, status, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (chunks >= kReduceChunks) {
       constexpr int kQ4 = (D * D + D) / 4;
-      pddp_reduce_kernel<D><<<dim3((kQ4 + kReduceThreads - 1) / kReduceThreads, slots, BH),
-                              kReduceThreads, 0, stream>>>(partials, N, C, d, slots, chunks);
+      pddp_reduce_kernel<D><<<dim3((kQ4 + kReduceThreads - 1) / kReduceThreads, nsplit, BH),
+                              kReduceThreads, 0, stream>>>(partials, tab, N, C, d, slots, chunks);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    pddp_power_kernel<D><<<dim3(slots, BH), kPowThreads, psmem, stream>>>(partials, N, C, d, slots,
-                                                                          chunks, iters, nodevec);
+    pddp_power_kernel<D><<<dim3(nsplit, BH), kPowThreads, psmem, stream>>>(
+        partials, tab, N, C, d, slots, chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     project<<<dim3((N + kProjThreads - 1) / kProjThreads, BH), kProjThreads, proj_smem_bytes<D>(),
               stream>>>(q, pa, N, d, slots, nodevec, keys, layout, H, head0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (max_node_rows(N, C, d) > kSmallNode) {
       if (max_node_rows(N, C, d) > kSplitWide)
-        pddp_split_kernel<1024, 8><<<dim3(slots, BH), 1024, 0, stream>>>(keys, pa, pb, N, C, d,
-                                                                         status);
+        pddp_split_kernel<1024, 8><<<dim3(nsplit, BH), 1024, 0, stream>>>(keys, pa, pb, tab, N, C,
+                                                                          d, status);
       else
-        pddp_split_kernel<256, 4><<<dim3(slots, BH), 256, 0, stream>>>(keys, pa, pb, N, C, d,
-                                                                       status);
+        pddp_split_kernel<256, 4><<<dim3(nsplit, BH), 256, 0, stream>>>(keys, pa, pb, tab, N, C, d,
+                                                                        status);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     pddp_split_small_kernel<<<dim3((slots + kSmallWarps - 1) / kSmallWarps, BH),
