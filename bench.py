@@ -87,13 +87,13 @@ def pddp_launches(N: int, C: int) -> int:
     """Kernel launches of one mcs_group call: init, the table of splitting
     nodes (when there is a depth) and finalize, then per depth moments, power
     iteration, projection and the warp-per-node split, plus the chunk-partial
-    reduction when a node has >= 4 chunks of 4096 rows and the block-per-node
+    reduction when a node has >= 4 chunks of 1024 rows and the block-per-node
     split when a node has > 1024 rows (pddp.cu)."""
     G = -(-N // C)
     nodes, count = [N], 2 + (1 if depths_of(G) > 0 else 0)
     for _ in range(depths_of(G)):
         mx = max(nodes)
-        count += 4 + (1 if -(-mx // 4096) >= 4 else 0) + (1 if mx > 1024 else 0)
+        count += 4 + (1 if -(-mx // 1024) >= 4 else 0) + (1 if mx > 1024 else 0)
         nxt = []
         for n in nodes:
             g = -(-n // C)

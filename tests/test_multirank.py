@@ -98,12 +98,12 @@ def test_head_slices_are_views_and_params_match():
 
 
 def test_pddp_launch_count_matches_the_launch_list():
-    # the large video workload's grouping: 10 depths x 4, the reduction at
-    # depths 0-2 (nodes of >= 4 chunks of 4096 rows), the block split at
-    # depths 0-6, init, node table, finalize; the 3D workload's nodes of 1024
+    # the large video workload's grouping launched 55 kernels in the ncu launch
+    # list of one call (10 depths x 4, reduce at depths 0-4, block split at
+    # depths 0-6, init, node table, finalize); the 3D workload's nodes of 1024
     # rows at depth 6 take the warp split only
-    assert bench.pddp_launches(75600, 128) == 3 + 40 + 3 + 7
-    assert bench.pddp_launches(65536, 64) == 3 + 40 + 3 + 6
+    assert bench.pddp_launches(75600, 128) == 55
+    assert bench.pddp_launches(65536, 64) == 3 + 40 + 5 + 6
     assert bench.pddp_launches(100, 128) == 2  # one group: no depth, no table
 
 

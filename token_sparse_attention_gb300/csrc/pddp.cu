@@ -38,7 +38,7 @@
 namespace mcs {
 namespace {
 
-constexpr int kChunkRows = 4096;  // rows per moments CTA (32 tiles of 128)
+constexpr int kChunkRows = 1024;  // rows per moments CTA (8 tiles of 128)
 constexpr int kMomProducers = 8;  // cp.async producer warps of the moments kernel (0-7)
 constexpr int kMomStages = 3;     // ring stages of the moments kernel (two CTAs per SM)
 constexpr int kMomMmaWarp = kMomProducers;
