@@ -625,6 +625,202 @@ __global__ void __launch_bounds__(kPowThreads, 2)
   }
 }
 
+// Power iteration for the depths whose nodes fit one moments chunk (the deep
+// levels, thousands of nodes).  The covariance is symmetric, so a node keeps
+// only its upper-triangle 8 x 8 blocks, one per thread (136 threads at
+// D = 128): half the registers of the full matrix, four nodes per SM instead
+// of two.  A step: block (a, b), a <= b, adds B v_b to rows 8a.. and, off the
+// diagonal, B^T v_a to rows 8b..; each contribution goes to its own slot of
+// a shared array part[row block][column block][8] (every slot written by
+// exactly one thread), and thread t < D sums row t's D/8 slots in column-block
+// order.  Normalisation, trace scaling and the sign rule as pddp_power_kernel.
+template <int D>
+constexpr int sym_threads() { return ((D / 8) * (D / 8 + 1) / 2 + 31) / 32 * 32; }
+
+template <int D>
+__global__ void __launch_bounds__(sym_threads<D>(), D == 128 ? 4 : 8)
+    pddp_power_sym_kernel(const float* __restrict__ partials, const int32_t* __restrict__ slot_tab,
+                          int N, int C, int depth, int slots, int max_chunks, int iters,
+                          float* __restrict__ nodevec) {
+  constexpr int NB = D / 8;                 // block rows
+  constexpr int NBLK = NB * (NB + 1) / 2;   // blocks of the upper triangle
+  constexpr int T = sym_threads<D>();
+  constexpr int kPad = NB * 8 + 8;          // floats per row block of part[] (bank spread)
+  constexpr int kNormEvery = 8;
+  constexpr int DD = D * D + D;
+  static_assert(D == 64 || D == 128, "D must be 64 or 128");
+  __shared__ __align__(16) float s[D];
+  __shared__ __align__(16) float vb[2][D];  // the iterate, double-buffered
+  __shared__ __align__(16) float part[NB * kPad];
+  __shared__ float red[T / 32];
+  __shared__ int lead;
+  const int slot = slot_tab[blockIdx.x], bh = blockIdx.y;
+  const Node nd = node_at(N, C, depth, slot);
+  if ((nd.n + C - 1) / C <= 1) return;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // this thread's block (a, b): row block a holds the NB - a blocks b = a .. NB-1
+  const bool has_blk = tid < NBLK;
+  int a = 0, b = 0;
+  if (has_blk) {
+    int t = tid;
+    while (t >= NB - a) {
+      t -= NB - a;
+      ++a;
+    }
+    b = a + t;
+  }
+  const bool diag = a == b;
+  const float* pc = partials + (size_t)(bh * slots + slot) * max_chunks * DD;  // one chunk
+  uint64_t B[8][4];  // rows 8a + i, columns 8b .. 8b + 7 as packed pairs
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (has_blk) {
+      const ulonglong2* r = reinterpret_cast<const ulonglong2*>(pc + (8 * a + i) * D + 8 * b);
+      const ulonglong2 x0 = __ldg(r), x1 = __ldg(r + 1);
+      B[i][0] = x0.x;
+      B[i][1] = x0.y;
+      B[i][2] = x1.x;
+      B[i][3] = x1.y;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) B[i][k] = 0ull;
+    }
+  }
+  float diag_v = 0.f;
+  if (tid < D) {
+    s[tid] = __ldg(pc + D * D + tid);
+    diag_v = __ldg(pc + tid * D + tid);
+    vb[0][tid] = rsqrtf(static_cast<float>(D));
+  }
+  __syncthreads();
+  const float inv_n = 1.f / static_cast<float>(nd.n);
+  // Cov = X^T X - s s^T / n
+  if (has_blk) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float sa = s[8 * a + i] * inv_n;
+      const uint64_t nsa = f2_pack(-sa, -sa);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        B[i][k] = f2_fma(nsa, f2_pack(s[8 * b + 2 * k], s[8 * b + 2 * k + 1]), B[i][k]);
+    }
+  }
+  // trace of Cov, then Cov / trace
+  if (tid < D) diag_v -= s[tid] * inv_n * s[tid];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) diag_v += __shfl_xor_sync(0xffffffffu, diag_v, o);
+  if (lane == 0) red[wid] = diag_v;
+  __syncthreads();
+  float tr = 0.f;
+#pragma unroll
+  for (int i = 0; i < T / 32; ++i) tr += red[i];
+  const float inv_tr = tr > 0.f ? 1.f / tr : 1.f;
+  const uint64_t itr2 = f2_pack(inv_tr, inv_tr);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) B[i][k] = f2_fma(B[i][k], itr2, 0ull);
+  int cur = 0;
+  for (int it = 0; it < iters; ++it) {
+    if (has_blk) {
+      const ulonglong2 p0 = *reinterpret_cast<const ulonglong2*>(vb[cur] + 8 * b);
+      const ulonglong2 p1 = *reinterpret_cast<const ulonglong2*>(vb[cur] + 8 * b + 4);
+      const uint64_t vbp[4] = {p0.x, p0.y, p1.x, p1.y};
+      float y1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint64_t acc = 0ull;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc = f2_fma(B[i][k], vbp[k], acc);
+        float lo, hi;
+        f2_unpack(acc, lo, hi);
+        y1[i] = lo + hi;
+      }
+      float* dst = part + a * kPad + b * 8;
+      *reinterpret_cast<float4*>(dst) = make_float4(y1[0], y1[1], y1[2], y1[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(y1[4], y1[5], y1[6], y1[7]);
+      if (!diag) {
+        const float4 q0 = *reinterpret_cast<const float4*>(vb[cur] + 8 * a);
+        const float4 q1 = *reinterpret_cast<const float4*>(vb[cur] + 8 * a + 4);
+        const float va[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint64_t y2[4] = {0ull, 0ull, 0ull, 0ull};  // columns 8b + 2k, 8b + 2k + 1
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t vi = f2_pack(va[i], va[i]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) y2[k] = f2_fma(B[i][k], vi, y2[k]);
+        }
+        float z[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f2_unpack(y2[k], z[2 * k], z[2 * k + 1]);
+        float* dst2 = part + b * kPad + a * 8;
+        *reinterpret_cast<float4*>(dst2) = make_float4(z[0], z[1], z[2], z[3]);
+        *reinterpret_cast<float4*>(dst2 + 4) = make_float4(z[4], z[5], z[6], z[7]);
+      }
+    }
+    __syncthreads();
+    if (tid < D) {
+      const float* src = part + (tid >> 3) * kPad + (tid & 7);
+      float y = 0.f;
+#pragma unroll
+      for (int c = 0; c < NB; ++c) y += src[c * 8];
+      vb[cur ^ 1][tid] = y;
+    }
+    __syncthreads();
+    cur ^= 1;
+    if (it == 0 || (it + 1) % kNormEvery == 0 || it == iters - 1) {
+      const float x = tid < D ? vb[cur][tid] : 0.f;
+      float sq = x * x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      __syncthreads();  // every thread has read red[] of the trace step or of the last norm
+      if (lane == 0) red[wid] = sq;
+      __syncthreads();
+      float norm2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < T / 32; ++i) norm2 += red[i];
+      if (norm2 == 0.f) {  // uniform: C v = 0, keep the previous vector
+        cur ^= 1;
+        break;
+      }
+      const float inv = rsqrtf(norm2);
+      if (tid < D) vb[cur][tid] = x * inv;
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  const float* v = vb[cur];
+  if (wid == 0) {  // largest |v_d|, lowest d on ties
+    float bv = -1.f;
+    int bi = 0;
+#pragma unroll
+    for (int k = lane; k < D; k += 32) {
+      const float x = fabsf(v[k]);
+      if (x > bv) {
+        bv = x;
+        bi = k;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > bv || (ob == bv && oi < bi)) {
+        bv = ob;
+        bi = oi;
+      }
+    }
+    if (lane == 0) lead = bi;
+  }
+  __syncthreads();
+  const float sign = v[lead] < 0.f ? -1.f : 1.f;
+  float* out = nodevec + (size_t)(bh * slots + slot) * 2 * D;
+  if (tid < D) {
+    out[tid] = sign * v[tid];
+    out[D + tid] = s[tid] * inv_n;  // mean
+  }
+}
+
 // ---------------------------------------------------------------- projection
 
 constexpr int kProjThreads = 32;  // one warp per CTA: a finished warp's slot is refilled at once
@@ -1093,8 +1289,12 @@ cudaError_t run_pddp(const __nv_bfloat16* q, int layout, int H, int head0,
                               kReduceThreads, 0, stream>>>(partials, tab, N, C, d, slots, chunks);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    pddp_power_kernel<D><<<dim3(nsplit, BH), kPowThreads, psmem, stream>>>(
-        partials, tab, N, C, d, slots, chunks, iters, nodevec);
+    if (chunks == 1)  // every node in one chunk: the half-matrix kernel, four nodes per SM
+      pddp_power_sym_kernel<D><<<dim3(nsplit, BH), sym_threads<D>(), 0, stream>>>(
+          partials, tab, N, C, d, slots, chunks, iters, nodevec);
+    else
+      pddp_power_kernel<D><<<dim3(nsplit, BH), kPowThreads, psmem, stream>>>(
+          partials, tab, N, C, d, slots, chunks, iters, nodevec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     project<<<dim3((N + kProjThreads - 1) / kProjThreads, BH), kProjThreads, proj_smem_bytes<D>(),
               stream>>>(q, pa, N, d, slots, nodevec, keys, layout, H, head0);
