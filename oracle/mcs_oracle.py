@@ -32,6 +32,11 @@ the site and the section:
                     high-mass tokens".
 * [ai.info/Find]    ai.info AI summary, section "Main Findings" (recall and
                     relative L1 of the selectors at matched density).
+* [ai.info/Future]  ai.info AI summary, section "Future Directions" (a
+                    comparison with low-precision attention left open).
+* [OFP8]            the OCP 8-bit floating point specification, format E4M3
+                    (not one of the pages: it defines the bytes of an fp8
+                    K/V cache).
 
 Readings taken where the pages are silent (each repeated at its function):
 softmax scale 1/sqrt(D); natural-log LSE; PDDP centred covariance, power
@@ -74,6 +79,9 @@ __all__ = [
     "per_query_select",
     "retained_mass",
     "rel_l1",
+    "e4m3_decode",
+    "e4m3_encode",
+    "sparse_attention_e4m3",
 ]
 
 
@@ -434,3 +442,62 @@ def rel_l1(got, want) -> float:
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     return float(np.abs(got - want).sum() / np.abs(want).sum())
+
+
+# ---------------------------------------------------------------------------
+# fp8 (E4M3) K/V cache  [ai.info/Future], [OFP8]
+# ---------------------------------------------------------------------------
+# The pages leave attention over low-precision K/V open [ai.info/Future].  The
+# library can hold K and V as E4M3 bytes with one scale per tensor:
+# k = k_scale * decode(k8).  E4M3 [OFP8]: sign bit, 4 exponent bits (bias 7),
+# 3 mantissa bits; exponent field 0 holds the subnormals m * 2**-9; no
+# infinities; S.1111.111 is NaN, so the largest finite magnitude is
+# 1.75 * 2**8 = 448.  Readings: a value is divided by its scale in float32
+# (one correctly rounded division), rounded to the nearest E4M3 value with
+# ties to the even mantissa, and magnitudes above 448 saturate to 448; NaN
+# becomes the code 0x7F.
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of E4M3 codes (uint8), as float64 (NaN for the NaN codes)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x, scale: float) -> np.ndarray:
+    """E4M3 codes of x / scale: the quotient taken in float32, then rounded to
+    the nearest E4M3 value (ties to even), saturating at +-448."""
+    r = np.asarray(x, dtype=np.float32) / np.float32(scale)
+    a = np.abs(r).astype(np.float64)
+    sign = np.signbit(r).astype(np.int64) << 7
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # subnormal range: multiples of 2**-9; 8 * 2**-9 is the smallest normal,
+    # whose code (exponent 1, mantissa 0) is also 8
+    code[sub] = np.rint(a[sub] / 2.0 ** -9).astype(np.int64)
+    nrm = ~sub & (a < 448.0)
+    _, e2 = np.frexp(a[nrm])            # a = f * 2**e2, 0.5 <= f < 1
+    e = e2 - 1                          # a in [2**e, 2**(e+1))
+    m = np.rint(a[nrm] / np.ldexp(1.0, e - 3)).astype(np.int64)  # 8 .. 16
+    up = m == 16
+    e = np.where(up, e + 1, e)
+    m = np.where(up, 8, m)
+    code[nrm] = np.minimum(((e + 7) << 3) | (m - 8), 0x7E)
+    code[~sub & ~nrm] = 0x7E            # >= 448: saturate
+    code = code | sign
+    code[np.isnan(r)] = 0x7F
+    return code.astype(np.uint8)
+
+
+def sparse_attention_e4m3(q, k8, v8, k_scale: float, v_scale: float, perm, idx, C: int,
+                          scale, groups=None):
+    """Token-sparse attention of one head over an E4M3 K/V cache: the method's
+    sparse attention [wisp/Tile] applied to the values the bytes stand for,
+    k = k_scale * decode(k8) and v = v_scale * decode(v8) [ai.info/Future]."""
+    k = k_scale * e4m3_decode(k8)
+    v = v_scale * e4m3_decode(v8)
+    return sparse_attention(q, k, v, perm, idx, C, scale, groups=groups)

@@ -455,3 +455,90 @@ def test_rel_l1_closed_forms():
     assert orc.rel_l1(2 * w, w) == pytest.approx(1.0)
     assert orc.rel_l1(np.zeros_like(w), w) == pytest.approx(1.0)
     assert orc.rel_l1(w + 0.5, w) == pytest.approx(0.5 * w.size / np.abs(w).sum())
+
+
+# ---------------------------------------------------------------- E4M3 K/V cache
+
+def _torch_e4m3(x):
+    """torch's float32 -> float8_e4m3fn conversion (round to nearest even)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.isnan(got).sum() == 2                      # S.1111.111 only
+    fin = ~np.isnan(got)
+    assert np.array_equal(got[fin], want[fin])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert got[0x38] == 1.0 and got[0xB8] == -1.0
+
+
+def test_e4m3_encode_matches_torch_rounding_including_ties():
+    table = orc.e4m3_decode(np.arange(0x7F, dtype=np.uint8))   # 0 .. 448, ascending
+    assert np.all(np.diff(table) > 0)
+    mids = (table[:-1] + table[1:]) / 2                        # exact ties (float32)
+    rng = _rng(60)
+    x = np.concatenate([
+        table, -table, mids, -mids,
+        rng.standard_normal(20000) * 20.0,
+        rng.standard_normal(5000) * 0.01,
+        np.ldexp(rng.uniform(0.5, 1.0, 5000), rng.integers(-14, 9, 5000)),
+    ]).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    assert np.array_equal(orc.e4m3_encode(x, 1.0), _torch_e4m3(x))
+    # ties go to the even mantissa: 1 + 1/16 -> 1.0, 1 + 3/16 -> 1.25
+    assert list(orc.e4m3_encode(np.array([1.0625, 1.1875], np.float32), 1.0)) == [0x38, 0x3A]
+
+
+def test_e4m3_encode_saturates_and_keeps_signs():
+    x = np.array([448.0, 449.0, 464.0, 479.0, 480.0, 1e6, -500.0, -1e30], np.float32)
+    assert list(orc.e4m3_encode(x, 1.0)) == [0x7E] * 6 + [0xFE] * 2
+    z = orc.e4m3_encode(np.array([0.0, -0.0, 2.0 ** -11, -2.0 ** -11, np.nan], np.float32), 1.0)
+    assert list(z) == [0x00, 0x80, 0x00, 0x80, 0x7F]
+    # the smallest subnormal and half of it (a tie between 0 and 2**-9: to even, 0)
+    assert list(orc.e4m3_encode(np.array([2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10], np.float32),
+                                1.0)) == [0x01, 0x00, 0x02]
+
+
+def test_e4m3_round_trip_and_scale():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], np.uint8)
+    vals = orc.e4m3_decode(codes)
+    assert np.array_equal(orc.e4m3_encode(vals.astype(np.float32), 1.0), codes)
+    # a power-of-two scale moves every finite value exactly: x = s * v encodes to v's code
+    for s in (0.125, 4.0):
+        inner = codes[np.abs(vals) * max(s, 1.0) <= 448.0]
+        v = orc.e4m3_decode(inner)
+        assert np.array_equal(orc.e4m3_encode((s * v).astype(np.float32), s), inner)
+    # the quotient is a float32 division: 1/3 of 3 in float32 is exactly 1
+    assert orc.e4m3_encode(np.array([3.0], np.float32), 3.0)[0] == 0x38
+
+
+def test_sparse_attention_e4m3_is_sparse_attention_of_the_decoded_cache():
+    rng = _rng(61)
+    N, D, C, K = 96, 16, 32, 24
+    q = _bf16(rng.standard_normal((N, D)))
+    # K/V that are exactly k_scale/v_scale times E4M3 values decode to themselves
+    k8 = rng.integers(0, 0x7E, (N, D)).astype(np.uint8) | (rng.integers(0, 2, (N, D)) << 7).astype(np.uint8)
+    v8 = rng.integers(0x20, 0x50, (N, D)).astype(np.uint8)
+    ks, vs = 0.0078125, 0.5
+    k = ks * orc.e4m3_decode(k8)
+    v = vs * orc.e4m3_decode(v8)
+    perm = np.arange(N)
+    idx = np.stack([np.sort(rng.choice(N, K, replace=False)) for _ in range(N // C)])
+    scale = orc.default_scale(D)
+    got = orc.sparse_attention_e4m3(q, k8, v8, ks, vs, perm, idx, C, scale)
+    want = orc.sparse_attention(q, k, v, perm, idx, C, scale)
+    assert np.array_equal(got, want)
+    # and the encoder recovers those bytes from the values
+    assert np.array_equal(orc.e4m3_encode(k.astype(np.float32), ks), k8)
+    # per group: softmax over the group's own selected rows (SDPA on the subset)
+    for g in range(N // C):
+        rows = perm[g * C:(g + 1) * C]
+        t = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[rows])[None], torch.from_numpy(k[idx[g]])[None],
+            torch.from_numpy(v[idx[g]])[None], scale=scale)[0].numpy()
+        assert np.allclose(got[rows], t, rtol=1e-10, atol=1e-12)
