@@ -483,6 +483,9 @@ def run_gpu(args, w, K, rank, world, dist):
     extra = None
     if world == 1 and not args.no_workloads:
         extra = run_schedules(dev)
+    e4m3 = None
+    if world == 1 and not args.no_e4m3:
+        e4m3 = e4m3_pass(mcs, p, reuse_in, perm, idx, res, out, stream)
     if rank != 0:
         return
 
@@ -512,6 +515,11 @@ def run_gpu(args, w, K, rank, world, dist):
         # algorithmic bytes per depth: Q read twice (moments, projection) and
         # the index traffic (perm read, keys written and read), 2-D x 2 + 3 x 4
         # bytes per token and head
+        # the same reuse launches over an E4M3 K/V cache (outside the timed
+        # step; None with --no-e4m3 or on several ranks)
+        "sparse_attn_e4m3(reuse)": (
+            dict(e4m3, tflops=tflops(flops_sparse, e4m3["ms"]),
+                 frac=tflops(flops_sparse, e4m3["ms"]) / peak) if e4m3 else None),
         "pddp": {"ms": stage_ms["pddp"], "depths": depths_of(G),
                  "algorithmic_gb": pddp_bytes(BH, w.N, w.D, G) / 1e9,
                  "gbs": pddp_bytes(BH, w.N, w.D, G) / (stage_ms["pddp"] * 1e-3) / 1e9,
@@ -602,6 +610,50 @@ def run_gpu(args, w, K, rank, world, dist):
     if extra is not None:
         line["workloads"] = extra
     print(json.dumps(line), flush=True)
+
+
+def e4m3_pass(mcs, p, reuse_in, perm, idx, res, out, stream, rounds=3):
+    """The reuse launches with K and V held as E4M3 bytes (one amax scale per
+    tensor), timed beside the bf16 launches on the same inputs and metadata,
+    alternating, after one warm-up round.  Returns the mean launch times, the
+    ratio, the quantisation time of one step's K and V, and the K/V bytes the
+    gathers read per launch."""
+    cached = []
+    for q_, k_, v_ in reuse_in:
+        ks = float(k_.float().abs().max().item()) / 448.0
+        vs = float(v_.float().abs().max().item()) / 448.0
+        k8 = torch.empty(k_.shape, dtype=torch.uint8, device=k_.device)
+        v8 = torch.empty_like(k8)
+        qa, qb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        qa.record(stream)
+        mcs.mcs_quantize_e4m3(k_, ks, k8)
+        mcs.mcs_quantize_e4m3(v_, vs, v8)
+        qb.record(stream)
+        cached.append((q_, k_, v_, k8, v8, ks, vs, qa, qb))
+    pairs = []  # (e4m3 launch, bf16 launch) events per input set and round
+    for rnd in range(rounds + 1):
+        for q_, k_, v_, k8, v8, ks, vs, _, _ in cached:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            mcs.mcs_sparse_attn_e4m3(p, q_, k8, v8, ks, vs, perm, idx, res, out)
+            ev[1].record(stream)
+            mcs.mcs_sparse_attn(p, q_, k_, v_, perm, idx, res, out)
+            ev[2].record(stream)
+            if rnd > 0:
+                pairs.append(ev)
+    torch.cuda.synchronize()
+    st = mcs.mcs_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the e4m3 pass: {mcs.mcs_status_string(st)}")
+    ms8 = statistics.mean(e[0].elapsed_time(e[1]) for e in pairs)
+    ms16 = statistics.mean(e[1].elapsed_time(e[2]) for e in pairs)
+    quant_ms = statistics.mean(c[7].elapsed_time(c[8]) for c in cached)
+    BH, G = p.B * p.H, p.G
+    return {"ms": ms8, "bf16_ms_same_run": ms16, "vs_bf16": ms16 / ms8,
+            "quantize_kv_ms": quant_ms,
+            "kv_gather_gb_per_launch": 2.0 * BH * G * p.K * p.D * 1 / 1e9,
+            "bf16_kv_gather_gb_per_launch": 2.0 * BH * G * p.K * p.D * 2 / 1e9,
+            "launches": len(pairs), "scales": "one amax scale per tensor (K, V)"}
 
 
 # The workloads' denoising schedules (single GPU), each density measured on its
@@ -859,6 +911,8 @@ def main():
     ap.add_argument("--split", default="weak", choices=["weak", "strong"],
                     help="several GPUs: weak = each rank a full copy of the workload's heads "
                          "(global batch grows), strong = the workload's heads split over ranks")
+    ap.add_argument("--no-e4m3", action="store_true",
+                    help="skip the reuse launches over an E4M3 K/V cache")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload schedule measurements (single GPU only)")
     ap.add_argument("--heads", type=int, default=0,

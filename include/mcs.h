@@ -181,6 +181,35 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
                                   const void* dense_out, void* residual, cudaStream_t stream);
 
 /*
+ * E4M3 K/V cache for the token-sparse step.  The pages leave attention over
+ * low-precision operands open (ai.info AI summary, "Future Directions",
+ * comparability with low-precision attention); this is the library's form of
+ * it.  E4M3 is the OCP 8-bit floating point format: sign, 4 exponent bits
+ * (bias 7), 3 mantissa bits, no infinities, largest finite magnitude 448.
+ *
+ * mcs_quantize_e4m3: x8[i] = E4M3(x[i] / scale) for n bf16 values: the
+ *   quotient in fp32 (correctly rounded), rounded to the nearest E4M3 value
+ *   (ties to even), magnitudes above 448 saturating to +-448, NaN to a NaN
+ *   code.  x (bf16) and x8 (bytes) are device buffers, 16-byte aligned; any
+ *   n (0 launches nothing).  scale > 0 and finite, else
+ *   MCS_ERR_INVALID_ARG.
+ * mcs_sparse_attn_e4m3: mcs_sparse_attn with K and V read from E4M3 bytes
+ *   k8, v8 (same shape and layout as k and v, one byte per element, 16-byte
+ *   aligned) standing for k = k_scale * k8 and v = v_scale * v8 (one scale
+ *   per tensor, > 0 and finite).  The products run on f16 operands: q is
+ *   converted from bf16 to f16 (exact inside the f16 range; magnitudes above
+ *   65504 saturate), the K and V values are exact in f16, and the attention
+ *   weights are rounded to f16.  residual NULL: out = O'; else out = O' +
+ *   residual.  Same shapes, checks and device status as mcs_sparse_attn.
+ */
+mcs_status mcs_quantize_e4m3(const void* x, size_t n, float scale, void* x8,
+                             cudaStream_t stream);
+mcs_status mcs_sparse_attn_e4m3(const mcs_params* p, const void* q, const void* k8,
+                                const void* v8, float k_scale, float v_scale,
+                                const int32_t* perm, const int32_t* idx, const void* residual,
+                                void* out, cudaStream_t stream);
+
+/*
  * Sibling-pair key lists for C = 64 groups: a kernel layout of idx, not a
  * step of the method.  A C = 64 group fills half of the 128-row query tile of
  * the tensor-core MMA, and a 64-row MMA takes as long as a 128-row one.

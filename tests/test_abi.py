@@ -163,3 +163,32 @@ def test_pair_lists_host_checks(L):
     assert L.mcs_sparse_attn_pairs(ctypes.byref(p), 16, 16, 16, 16, None, None, 16, None) == 1
     assert L.mcs_sparse_attn_pairs_record(ctypes.byref(p), 16, 16, 16, 16, 256, None, 16,
                                           None) == 1  # record needs dense_out
+
+
+def test_e4m3_entries_reject_bad_arguments(L):
+    f = ctypes.c_float
+    # quantize: null or misaligned buffers, bad scales; n = 0 launches nothing
+    assert L.mcs_quantize_e4m3(None, 16, f(1.0), 16, None) == 1
+    assert L.mcs_quantize_e4m3(16, 16, f(1.0), 24, None) == 1
+    assert L.mcs_quantize_e4m3(16, 16, f(0.0), 16, None) == 1
+    assert L.mcs_quantize_e4m3(16, 16, f(float("inf")), 16, None) == 1
+    assert L.mcs_quantize_e4m3(None, 0, f(1.0), None, None) == 0
+    # sparse attention over E4M3 K/V: the shape checks of mcs_sparse_attn,
+    # then pointers, alignment and scales
+    p = mcs.params(1, 2, 256, 96, 64, 40)
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 16, f(1), f(1), 16, 16, None, 16,
+                                  None) == 2
+    p = mcs.params(1, 2, 256, 128, 64, 0)
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 16, f(1), f(1), 16, 16, None, 16,
+                                  None) == 1
+    p = mcs.params(1, 2, 256, 128, 64, 40)
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, None, 16, f(1), f(1), 16, 16, None, 16,
+                                  None) == 1
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 40, f(1), f(1), 16, 16, None, 16,
+                                  None) == 1
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 16, f(0), f(1), 16, 16, None, 16,
+                                  None) == 1
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 16, f(1), f(-2), 16, 16, None, 16,
+                                  None) == 1
+    assert L.mcs_sparse_attn_e4m3(ctypes.byref(p), 16, 16, 16, f(1), f(1), 16, 16, 24, 16,
+                                  None) == 1

@@ -37,6 +37,16 @@
 // row's running max grows by more than 16, so P <= 2^16; P is bf16 (relative
 // rounding whatever its size) and O and the row sums are fp32, whose range
 // that bound leaves untouched: 2^16 * N * |v| stays far below 2^127).
+//
+// E4M3 K/V (mode flag kE4M3; the pages leave low-precision attention open:
+// ai.info AI summary, "Future Directions"): K and V are read as E4M3 bytes,
+// half the bytes of bf16.  The producers load 16 bytes of a row into
+// registers, convert them to f16 (exact: every E4M3 value is an f16 value)
+// and store 32 bytes into the same swizzled layout; Q is converted from bf16
+// to f16 on its way in, P is written as f16, and the MMAs take f16 operands
+// (kind::f16, both operands f16).  P <= 2^15 there (rescale threshold 15),
+// inside the f16 range.  The K scale is folded into the softmax scale, the V
+// scale into the output normalisation.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -51,6 +61,7 @@ constexpr int kFirstProducer = kSoftmaxWarps;
 constexpr int kMmaWarp = kFirstProducer + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kRescaleThreshold = 16.0f;
+constexpr float kRescaleThresholdF16 = 15.0f;  // f16 P: 2^15 < 65504
 // Batch-completion barriers, used round robin.  A waiter on batch n reads the
 // phase parity of done[n % kDone]; that is unambiguous as long as batch
 // n + kDone cannot have completed yet.  The producers lag furthest: before
@@ -145,6 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = AttnLayout<D, kPairs>;
   constexpr int NS = L::kStages;
   constexpr bool kSparseMode = MODE != kDense;
+  constexpr bool kE4 = (MODE & kE4M3) != 0;
+  static_assert(!kE4 || (!kPairs && (kBase == kSparse || kBase == kSparseAdd)),
+                "E4M3 K/V: unpaired sparse and sparse + residual modes only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -288,16 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of a tile's rows are read once per warp (one index per lane) and
       // broadcast with shuffles.
       constexpr int kPT = 32 * kProducers;
-      constexpr int kSegs = D * 2 / 16;                 // 16-byte segments per row
+      constexpr int kSegs = D * 2 / 16;                 // 16-byte segments per bf16 row
       constexpr int kChunks = BM * kSegs;
       constexpr int kPer = (kChunks + kPT - 1) / kPT;   // Q chunks per thread (at most)
-      constexpr int kRPI = 32 / kSegs;                  // rows per warp instruction
+      constexpr int kKVSegs = kE4 ? D / 16 : kSegs;     // 16-byte segments per K/V row read
+      constexpr int kRPI = 32 / kKVSegs;                // rows per warp instruction
       constexpr int kRG = BN / kRPI;                    // row groups per tile
       constexpr int kGPW = (kRG + kProducers - 1) / kProducers;  // row groups per warp
       static_assert(kGPW * kRPI <= 32, "one index per lane");
       const int tid = (warp - kFirstProducer) * 32 + lane;
       const int pw = warp - kFirstProducer;
-      const int sub = lane / kSegs, seg = lane % kSegs;
+      const int sub = lane / kKVSegs, seg = lane % kKVSegs;
       const int group[2] = {2 * pair, has_b ? 2 * pair + 1 : 2 * pair};
       bool bad = false;
       // Q rows of both units (perm order); padding slots, rows past the
@@ -307,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* perm_g =
             a.perm + (static_cast<size_t>(bh) * a.G + (kPairs ? 2 * group[x] : group[x])) * a.C;
         const int qrows = kPairs ? (2 * group[x] + 1 < a.G ? 2 : 1) * a.C : a.C;
+        [[maybe_unused]] uint4 qw[kE4 ? kPer : 1];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int c = tid + kPT * k;
@@ -317,11 +333,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tok >= a.N) { bad = true; tok = -1; }
             const __nv_bfloat16* src =
                 a.q + static_cast<size_t>(rm.rbase + (tok < 0 ? 0 : tok) * rm.rstride) * D + sg * 8;
-            cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, sg), src, tok >= 0);
+            if constexpr (kE4)  // bf16 -> f16 through registers: all loads first
+              qw[k] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(src))
+                               : make_uint4(0u, 0u, 0u, 0u);
+            else
+              cp_async16_zfill(qs + x * L::kTileBytes + swz_offset(r, sg), src, tok >= 0);
+          }
+        }
+        if constexpr (kE4) {
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int c = tid + kPT * k;
+            if (c < kChunks) {
+              const uint4 w = qw[k];
+              st_shared16(qs + x * L::kTileBytes + swz_offset(c / kSegs, c % kSegs),
+                          make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y),
+                                     bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w)));
+            }
           }
         }
       }
-      cp_async_arrive(q_full);
+      if constexpr (kE4) {
+        fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
+        mbar_arrive(q_full);
+      } else {
+        cp_async_arrive(q_full);
+      }
       // This lane's row (RowMap) of tile j of unit x: lane l < kGPW * kRPI
       // holds the row of group pw + kProducers * (l / kRPI), sub-row l % kRPI.
       // Loaded two tiles ahead so that the index latency (the index array is
@@ -383,6 +420,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int off = tid * 128; off < bytes; off += kPT * 128)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(idx_g + off));
       }
+      if constexpr (kE4) {
+        // E4M3 rows go through registers: the loads of the next ring item are
+        // issued before the current item (loaded one item earlier) is
+        // converted and stored, alternating two buffers.  Items in order:
+        // K_a(0) K_b(0), then per step j V_a(j) K_a(j+1) V_b(j) K_b(j+1)
+        // (V_a(j) V_b(j) on the last step); at the top of step j buffer A
+        // holds V_a(j).  (Fetching two or three items ahead, through a
+        // generic item sequence and three register buffers, measured slower.)
+        // per lane: the swizzled stage offsets of its two 16-byte f16 chunks
+        // in each of its row groups (fixed for the whole kernel)
+        int soff[kGPW][2];
+#pragma unroll
+        for (int i = 0; i < kGPW; ++i) {
+          const int r = (pw + kProducers * i) * kRPI + sub;
+          soff[i][0] = swz_offset(r, 2 * seg);
+          soff[i][1] = swz_offset(r, 2 * seg + 1);
+        }
+        const uint8_t* k8 = a.k8 + seg * 16;
+        const uint8_t* v8 = a.v8 + seg * 16;
+        auto fetch = [&](uint4 (&buf)[kGPW], const uint8_t* src, int rows) {
+#pragma unroll
+          for (int i = 0; i < kGPW; ++i) {
+            const int rg = pw + kProducers * i;
+            const int row = __shfl_sync(0xffffffffu, rows, i * kRPI + sub);
+            buf[i] = rg < kRG ? ld_global_nc16(src + static_cast<size_t>(row) * D)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          }
+        };
+        auto put = [&](int it, const uint4 (&buf)[kGPW]) -> bool {
+          const int st = it % NS;
+          if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
+          uint8_t* stage = ring + st * L::kStageBytes;
+#pragma unroll
+          for (int i = 0; i < kGPW; ++i) {
+            if (pw + kProducers * i < kRG) {
+              uint4 lo, hi;
+              e4m3x4_to_f16x4(buf[i].x, lo.x, lo.y);
+              e4m3x4_to_f16x4(buf[i].y, lo.z, lo.w);
+              e4m3x4_to_f16x4(buf[i].z, hi.x, hi.y);
+              e4m3x4_to_f16x4(buf[i].w, hi.z, hi.w);
+              st_shared16(stage + soff[i][0], lo);
+              st_shared16(stage + soff[i][1], hi);
+            }
+          }
+          fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
+          mbar_arrive(full + st);
+          ++issued;
+          return true;
+        };
+        int bits;  // group bits: paired mode only
+        int r0[2], r1[2] = {0, 0}, r2[2] = {0, 0};
+        r0[0] = load_rows(0, 0, &bits);
+        r0[1] = load_rows(1, 0, &bits);
+        if (nkv > 1) {
+          r1[0] = load_rows(0, 1, &bits);
+          r1[1] = load_rows(1, 1, &bits);
+        }
+        uint4 bufA[kGPW], bufB[kGPW];
+        fetch(bufA, k8, r0[0]);
+        fetch(bufB, k8, r0[1]);
+        bool ok = put(k_item(0, 0), bufA);
+        fetch(bufA, v8, r0[0]);
+        ok = ok && put(k_item(1, 0), bufB);
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (a.fault && j >= 1) break;  // test-only: starve the MMA warp
+          const bool more = j + 1 < nkv;
+          // indices of tile j+2, a step before their first use
+          if (j + 2 < nkv) {
+            r2[0] = load_rows(0, j + 2, &bits);
+            r2[1] = load_rows(1, j + 2, &bits);
+          }
+          if (more) {
+            fetch(bufB, k8, r1[0]);                    // K_a(j+1)
+            ok = put(v_item(0, j), bufA);                // V_a(j)
+            if (ok) {
+              fetch(bufA, v8, r0[1]);                  // V_b(j)
+              ok = put(k_item(0, j + 1), bufB);          // K_a(j+1)
+            }
+            if (ok) {
+              fetch(bufB, k8, r1[1]);                  // K_b(j+1)
+              ok = put(v_item(1, j), bufA);              // V_b(j)
+            }
+            if (ok) {
+              fetch(bufA, v8, r1[0]);                  // V_a(j+1)
+              ok = put(k_item(1, j + 1), bufB);          // K_b(j+1)
+            }
+          } else {
+            fetch(bufB, v8, r0[1]);                    // V_b(j)
+            ok = put(v_item(0, j), bufA) && put(v_item(1, j), bufB);
+          }
+          r0[0] = r1[0];
+          r0[1] = r1[1];
+          r1[0] = r2[0];
+          r1[1] = r2[1];
+        }
+      } else {
       // rows (and paired-mode group bits) of tiles j (V_x(j)), j+1 (K_x(j+1))
       // and j+2 (being fetched)
       int r0[2], r1[2] = {0, 0}, r2[2] = {0, 0};
@@ -416,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         b1[0] = b2[0];
         b1[1] = b2[1];
       }
+      }
       if (bad) atomicOr(a.status, DEV_BOUNDS);
       if (*abort_flag) asm volatile("cp.async.wait_all;" ::: "memory");  // copies land first
     }
@@ -431,8 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and QK_x(j+1) of a unit are therefore issued as one batch, after the
     // waits for its operands (V_x(j) and K_x(j+1), loaded well ahead) and for
     // P_x(j).
-    constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
+    constexpr uint32_t idesc_qk =
+        kE4 ? idesc_f16(BM, BN, false, false) : idesc_bf16(BM, BN, false, false);
+    constexpr uint32_t idesc_pv = kE4 ? idesc_f16(BM, D, false, true) : idesc_bf16(BM, D, false, true);
     const uint32_t ring_addr = smem_u32(ring);
     const uint32_t q_addr = smem_u32(qs);
     auto stage_addr = [&](int item) { return ring_addr + (item % NS) * L::kStageBytes; };
@@ -559,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp-collective, so the whole warp enters the rescale when any of its
       // rows needs it (f = 1 for the others).  PV_x(j-1) has completed: it
       // was issued before QK_x(j), whose completion this warp has seen.
-      const bool need = (j > 0) && (m_new > m_run + kRescaleThreshold);
+      const bool need = (j > 0) && (m_new > m_run + (kE4 ? kRescaleThresholdF16 : kRescaleThreshold));
       if (j == 0) m_run = m_new;
       if (__any_sync(0xffffffffu, need)) {
         const float f = need ? ex2(m_run - m_new) : 1.f;
@@ -602,10 +737,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), c2, nm2), x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
-            pk[i] = pack_bf16(p0, p1);
+            pk[i] = kE4 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
             accf[i & 3] = f2_add(accf[i & 3], f2_pack(p0, p1));
-            accb[i & 3] = f2_add(accb[i & 3], f2_pack(__uint_as_float(pk[i] << 16),
-                                                      __uint_as_float(pk[i] & 0xFFFF0000u)));
+            if constexpr (kE4) {
+              const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+              accb[i & 3] = f2_add(accb[i & 3], f2_pack(r.x, r.y));
+            } else {
+              accb[i & 3] = f2_add(accb[i & 3], f2_pack(__uint_as_float(pk[i] << 16),
+                                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+            }
           }
           tmem_st16(tS + h * 32 + c * 16, pk);
         }
@@ -620,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && wait_batch(2 * nkv + x - 1)) {  // the last PV_x complete
       tc_fence_after();
-      const float inv_l = 1.f / l_b16;
+      const float inv_l = (kE4 ? a.v_scale : 1.f) / l_b16;
       const int unit = 2 * pair + x;
       int token;
       if (!kSparseMode) {
@@ -726,6 +866,10 @@ cudaError_t launch_attention(int D, int mode, const CUtensorMap* tq, const CUten
   MCS_ATTN_CASE(64, kSparse | kPaired)
   MCS_ATTN_CASE(64, kSparseAdd | kPaired)
   MCS_ATTN_CASE(64, kSparseRecord | kPaired)
+  MCS_ATTN_CASE(128, kSparse | kE4M3)
+  MCS_ATTN_CASE(128, kSparseAdd | kE4M3)
+  MCS_ATTN_CASE(64, kSparse | kE4M3)
+  MCS_ATTN_CASE(64, kSparseAdd | kE4M3)
 #undef MCS_ATTN_CASE
   return cudaErrorInvalidValue;
 }

@@ -48,6 +48,7 @@ enum AttnMode : int {
   kSparseAdd = 2,     // token-sparse attention + cached residual (reuse step)
   kSparseRecord = 3,  // token-sparse attention, writes residual = dense_out - O' (anchor)
   kPaired = 4,        // flag on a sparse mode: C = 64 sibling pairs over their key unions
+  kE4M3 = 8,          // flag on kSparse / kSparseAdd: K and V are E4M3 bytes (k8, v8)
 };
 
 // Sibling-pair key lists (C = 64): groups 2u and 2u+1 of a head form pair u
@@ -89,6 +90,11 @@ struct AttnArgs {
   const __nv_bfloat16* v;        // [BH, N, D]
   unsigned* status;              // device status word
   int fault;                     // test-only: 1 = producers stop after the first K/V tile
+  // kE4M3: K and V as E4M3 bytes [BH, N, D] (rows as for k, v); the K scale
+  // is folded into scale_log2, the V scale multiplies the output
+  const uint8_t* k8;
+  const uint8_t* v8;
+  float v_scale;
   // kPaired: pair lists (see PairLayout)
   int P, cap;
   const int32_t* plen;           // [BH, P]
@@ -133,6 +139,10 @@ cudaError_t launch_topk(const float* mass, const uint32_t* hist, int rows, int n
 // idx [BH, G, K] (rows ascending) -> pair lists in `pairs` (PairLayout).
 cudaError_t launch_pair_union(const int32_t* idx, int BH, int G, int K, int N, void* pairs,
                               unsigned* status, cudaStream_t stream);
+
+// x8[i] = E4M3(x[i] / scale) for n bf16 values (x and x8 16-byte aligned).
+cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, size_t n, float scale, uint8_t* x8,
+                                 cudaStream_t stream);
 
 // Device address of the library's status word (for kernels' status argument).
 cudaError_t device_status_word(unsigned** out);

@@ -366,6 +366,58 @@ mcs_status mcs_sparse_attn_record(const mcs_params* p, const void* q, const void
   return run_sparse(p, q, k, v, perm, idx, dense_out, residual, mcs::kSparseRecord, stream);
 }
 
+mcs_status mcs_quantize_e4m3(const void* x, size_t n, float scale, void* x8,
+                             cudaStream_t stream) {
+  if (n > 0 && (!x || !x8 || !aligned16(x) || !aligned16(x8))) return MCS_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return MCS_ERR_INVALID_ARG;
+  cudaError_t e = mcs::launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(x), n, scale,
+                                            static_cast<uint8_t*>(x8), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 quantize launch");
+  return MCS_OK;
+}
+
+mcs_status mcs_sparse_attn_e4m3(const mcs_params* p, const void* q, const void* k8,
+                                const void* v8, float k_scale, float v_scale,
+                                const int32_t* perm, const int32_t* idx, const void* residual,
+                                void* out, cudaStream_t stream) {
+  mcs_status s = check_shape(p, true);
+  if (s != MCS_OK) return s;
+  if (!q || !k8 || !v8 || !perm || !idx || !out) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k8) || !aligned16(v8) || !aligned16(out) ||
+      (residual && !aligned16(residual)))
+    return MCS_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+    return MCS_ERR_INVALID_ARG;
+  const int BH = p->B * p->H;
+  // the sparse modes read rows with plain loads; the maps are kernel
+  // parameters only
+  CUtensorMap tq;
+  if (!make_gather_map(&tq, q, BH, p->N, p->D))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(gather)");
+  mcs::AttnArgs a{};
+  a.H = p->H;
+  a.layout = p->layout;
+  a.N = p->N;
+  a.C = p->C;
+  a.G = groups_of(p);
+  a.K = p->K;
+  a.scale_log2 = scale_of(p) * kLog2e * k_scale;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.perm = perm;
+  a.idx = idx;
+  a.aux_in = static_cast<const __nv_bfloat16*>(residual);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k8 = static_cast<const uint8_t*>(k8);
+  a.v8 = static_cast<const uint8_t*>(v8);
+  a.v_scale = v_scale;
+  a.fault = fault_from_env();
+  if ((s = status_ptr(&a.status)) != MCS_OK) return s;
+  const int mode = (residual ? mcs::kSparseAdd : mcs::kSparse) | mcs::kE4M3;
+  cudaError_t e = mcs::launch_attention(p->D, mode, &tq, &tq, &tq, a, BH, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 sparse attention launch");
+  return MCS_OK;
+}
+
 size_t mcs_pair_bytes(const mcs_params* p) {
   if (check_pairs(p) != MCS_OK) return 0;
   return mcs::pair_layout(p->B * p->H, groups_of(p), p->K).total;

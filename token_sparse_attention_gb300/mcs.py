@@ -24,7 +24,8 @@ __all__ = [
     "mcs_anchor_select", "mcs_group_noalloc", "mcs_meta_bytes", "mcs_meta_offsets",
     "meta_views", "mcs_meta_pack", "mcs_meta_unpack", "Stager", "mcs_block_workspace", "mcs_block_topk", "mcs_pooled_block_select",
     "mcs_gather_mass", "mcs_rel_l1", "mcs_pair_bytes", "empty_pairs", "mcs_pair_lists",
-    "mcs_sparse_attn_pairs", "mcs_sparse_attn_pairs_record",
+    "mcs_sparse_attn_pairs", "mcs_sparse_attn_pairs_record", "mcs_quantize_e4m3",
+    "mcs_sparse_attn_e4m3",
 ]
 
 # Every symbol include/mcs.h declares.
@@ -37,6 +38,7 @@ EXPORTED = (
     "mcs_stager_create", "mcs_stager_destroy",
     "mcs_stager_prefetch", "mcs_stager_offload", "mcs_stager_wait", "mcs_block_workspace",
     "mcs_block_topk", "mcs_pooled_block_select", "mcs_gather_mass", "mcs_rel_l1",
+    "mcs_quantize_e4m3", "mcs_sparse_attn_e4m3",
 )
 
 STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED",
@@ -112,6 +114,9 @@ _SIGS = {
     "mcs_pooled_block_select": ([_pp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp], _st),
     "mcs_gather_mass": ([_pp, _vp, _i, _vp, _vp, _vp], _st),
     "mcs_rel_l1": ([_pp, _vp, _vp, _vp, _i, _vp, _vp], _st),
+    "mcs_quantize_e4m3": ([_vp, _sz, ctypes.c_float, _vp, _vp], _st),
+    "mcs_sparse_attn_e4m3": ([_pp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp,
+                              _vp, _vp, _vp], _st),
 }
 
 
@@ -251,6 +256,36 @@ def mcs_sparse_attn_record(p: Params, q, k, v, perm, idx, dense_out, residual, s
         _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
         _ptr(dense_out, bf, s, "dense_out"), _ptr(residual, bf, s, "residual"),
         _stream(stream)), "mcs_sparse_attn_record")
+
+
+def _bytes8(t, name, numel):
+    """E4M3 tensors: torch.float8_e4m3fn or their uint8 view."""
+    if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    ptr = _ptr(t, torch.uint8, None, name)
+    if t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} bytes, got {t.numel()}")
+    return ptr
+
+
+def mcs_quantize_e4m3(x, scale: float, x8, stream=None):
+    """x8 = E4M3(x / scale), elementwise (x bf16; x8 uint8 or float8_e4m3fn)."""
+    n = x.numel()
+    _check(lib().mcs_quantize_e4m3(_ptr(x, torch.bfloat16, None, "x"), n, float(scale),
+                                   _bytes8(x8, "x8", n), _stream(stream)), "mcs_quantize_e4m3")
+
+
+def mcs_sparse_attn_e4m3(p: Params, q, k8, v8, k_scale: float, v_scale: float, perm, idx,
+                         residual, out, stream=None):
+    bf, s = torch.bfloat16, _qkv_shape(p)
+    n = math.prod(s)
+    _check(lib().mcs_sparse_attn_e4m3(
+        ctypes.byref(p), _ptr(q, bf, s, "q"), _bytes8(k8, "k8", n), _bytes8(v8, "v8", n),
+        float(k_scale), float(v_scale),
+        _ptr(perm, torch.int32, (p.B, p.H, p.G * p.C), "perm"),
+        _ptr(idx, torch.int32, (p.B, p.H, p.G, p.K), "idx"),
+        _ptr(residual, bf, s, "residual", optional=True), _ptr(out, bf, s, "out"),
+        _stream(stream)), "mcs_sparse_attn_e4m3")
 
 
 def mcs_pair_bytes(p: Params) -> int:
