@@ -44,3 +44,37 @@ def test_withheld_load_times_out_and_context_survives(monkeypatch):
     want = orc.sparse_attention(P.f64(q[0, 0]), P.f64(k[0, 0]), P.f64(v[0, 0]), perm[0, 0],
                                 idx[0, 0], C, orc.default_scale(D))
     P.assert_close(out[0, 0], want, "sparse after a timed-out launch")
+
+
+def test_withheld_e4m3_load_times_out_and_context_survives(monkeypatch):
+    """The same for the E4M3 K/V path, whose producers stage rows through
+    registers instead of cp.async."""
+    mcs_build.build()
+    mcs.lib()
+    N, D, C, K = 512, 128, 128, 300
+    q, k, v = P.random_qkv(1, 1, N, D, seed=24)
+    perm = P.random_groups(N, C, 25)[None, None]
+    idx = P.random_idx(N, perm.shape[-1] // C, K, 26)[None, None]
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    ks = float(k.float().abs().max()) / 448.0
+    vs = float(v.float().abs().max()) / 448.0
+    k8 = torch.empty(kd.shape, dtype=torch.uint8, device="cuda")
+    v8 = torch.empty_like(k8)
+    mcs.mcs_quantize_e4m3(kd, ks, k8)
+    mcs.mcs_quantize_e4m3(vd, vs, v8)
+    pd = torch.from_numpy(perm.astype(np.int32)).cuda()
+    xd = torch.from_numpy(idx.astype(np.int32)).cuda()
+    p = mcs.params(1, 1, N, D, C, K)
+    out = torch.zeros_like(qd)
+    assert mcs.mcs_device_status() == 0
+    monkeypatch.setenv("MCS_TEST_FAULT", "stall_load")
+    mcs.mcs_sparse_attn_e4m3(p, qd, k8, v8, ks, vs, pd, xd, None, out)
+    assert mcs.mcs_device_status() == 5  # MCS_ERR_TIMEOUT
+    monkeypatch.delenv("MCS_TEST_FAULT")
+    mcs.mcs_sparse_attn_e4m3(p, qd, k8, v8, ks, vs, pd, xd, None, out)
+    assert mcs.mcs_device_status() == 0
+    ko = orc.e4m3_encode(k[0, 0].float().numpy(), ks)
+    vo = orc.e4m3_encode(v[0, 0].float().numpy(), vs)
+    want = orc.sparse_attention_e4m3(P.f64(q[0, 0]), ko, vo, ks, vs, perm[0, 0], idx[0, 0], C,
+                                     orc.default_scale(D))
+    P.assert_close(out[0, 0], want, "e4m3 sparse after a timed-out launch")
