@@ -52,9 +52,9 @@ TRAFFIC = {
     # ncu dram bytes (read + write) of the sparse reuse launch, captured on the
     # 4-head large workload (the timed step's first reuse launch of `bench.py
     # --heads 4 --steps 1 --warmup 1 --no-e2e --no-cpu-baseline
-    # --no-workloads`), times 10 for the 40-head launch: heads are independent
+    # --no-workloads --no-e4m3`), times 10 for the 40-head launch: heads are independent
     # and the grid scales with them
-    "attn.cu": {"sha": "34c2b542de82", "bytes_per_launch": 7315973120},
+    "attn.cu": {"sha": "2b6898439b1b", "bytes_per_launch": 7317790720},
 }
 
 
