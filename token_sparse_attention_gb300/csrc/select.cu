@@ -548,37 +548,42 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
       }
     };
     constexpr int kChunk = kPer * kTopkThreads;
+    // digit > d  <=>  bits >= hiT;  digit == d  <=>  loT <= bits < hiT (d is
+    // below the clamped top digit on this path); positions past n load 0 and
+    // are excluded only in the last, partial chunk
+    const uint32_t loT = d << 20, hiT = (d + 1u) << 20;
     uint32_t run_a = 0, run_c = 0;
     for (int base = 0; base < n; base += kChunk) {
       const int i0 = base + kPer * tid;
+      const bool tail = base + kChunk > n;
       uint32_t cur[kPer];
       load(i0, cur);
-      uint32_t na = 0, nc = 0;
+      uint32_t na = 0, nge = 0;
 #pragma unroll
       for (int e = 0; e < kPer; ++e) {
-        const bool valid = i0 + e < n;
-        const uint32_t dg = mass_digit(cur[e]);
-        na += (valid && dg > d) ? 1u : 0u;
-        nc += (valid && dg == d) ? 1u : 0u;
+        const bool valid = !tail || i0 + e < n;
+        na += (valid && cur[e] >= hiT) ? 1u : 0u;
+        nge += (valid && cur[e] >= loT) ? 1u : 0u;
       }
-      const uint32_t packed = (na << 16) | nc;
+      const uint32_t packed = (na << 16) | (nge - na);
       uint32_t tot;
       const uint32_t excl = block_inclusive_scan(packed, warp_sums, &tot) - packed;
       uint32_t pa = run_a + (excl >> 16), pc = run_c + (excl & 0xFFFFu);
+      if (nge != 0) {
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        if (i0 + e >= n) continue;
-        const uint32_t dg = mass_digit(cur[e]);
-        if (dg > d) {
-          if (pa < A) above[pa] = static_cast<uint32_t>(i0 + e);
-          ++pa;
-          acc += __uint_as_float(cur[e]);
-        } else if (dg == d) {
-          if (pc < M) {
-            ckey[pc] = cur[e];
-            cidx[pc] = static_cast<uint32_t>(i0 + e);
+        for (int e = 0; e < kPer; ++e) {
+          if (cur[e] < loT || (tail && i0 + e >= n)) continue;
+          if (cur[e] >= hiT) {
+            if (pa < A) above[pa] = static_cast<uint32_t>(i0 + e);
+            ++pa;
+            acc += __uint_as_float(cur[e]);
+          } else {
+            if (pc < M) {
+              ckey[pc] = cur[e];
+              cidx[pc] = static_cast<uint32_t>(i0 + e);
+            }
+            ++pc;
           }
-          ++pc;
         }
       }
       run_a += tot >> 16;
