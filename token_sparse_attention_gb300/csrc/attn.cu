@@ -40,9 +40,10 @@
 //
 // E4M3 K/V (mode flag kE4M3; the pages leave low-precision attention open:
 // ai.info AI summary, "Future Directions"): K and V are read as E4M3 bytes,
-// half the bytes of bf16.  The producers load 16 bytes of a row into
-// registers, convert them to f16 (exact: every E4M3 value is an f16 value)
-// and store 32 bytes into the same swizzled layout; Q is converted from bf16
+// half the bytes of bf16.  The producers copy the E4M3 rows into the stage
+// with cp.async, then read them back, convert them to f16 (exact: every E4M3
+// value is an f16 value) and store them in the same swizzled layout the bf16
+// gathers produce; Q is converted from bf16
 // to f16 on its way in, P is written as f16, and the MMAs take f16 operands
 // (kind::f16, both operands f16).  P <= 2^15 there (rescale threshold 15),
 // inside the f16 range.  The K scale is folded into the softmax scale, the V
@@ -421,52 +422,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(idx_g + off));
       }
       if constexpr (kE4) {
-        // E4M3 rows go through registers: the loads of the next ring item are
-        // issued before the current item (loaded one item earlier) is
-        // converted and stored, alternating two buffers.  Items in order:
-        // K_a(0) K_b(0), then per step j V_a(j) K_a(j+1) V_b(j) K_b(j+1)
-        // (V_a(j) V_b(j) on the last step); at the top of step j buffer A
-        // holds V_a(j).  (Fetching two or three items ahead, through a
-        // generic item sequence and three register buffers, measured slower.)
-        // per lane: the swizzled stage offsets of its two 16-byte f16 chunks
-        // in each of its row groups (fixed for the whole kernel)
-        int soff[kGPW][2];
+        // E4M3 rows: each ring item's rows are copied as raw bytes (16-byte
+        // cp.async, one commit group per item) into the upper half of their
+        // own f16 lines in the item's stage (D = 128: line r of the second
+        // 128-byte sub-tile; D = 64: bytes 64-127 of line r).  kLag items
+        // later, once they have landed, the same lanes read them back,
+        // convert them to f16 and store row r's f16 chunks into line r (and,
+        // D = 128, line r of the first sub-tile), then arrive on the stage.
+        // Only the lanes of row r touch its staging bytes and its lines, all
+        // in one warp, so a __syncwarp between the reads and the writes
+        // orders them.  The copies need no registers and run ahead like the
+        // bf16 gathers; the conversion waits kLag items behind them.
+        constexpr int kLag = 2;
+        int stoff[kGPW], soff[kGPW][2];
 #pragma unroll
         for (int i = 0; i < kGPW; ++i) {
           const int r = (pw + kProducers * i) * kRPI + sub;
+          stoff[i] = (D == 128 ? 128 * 128 : 64) + r * 128 + seg * 16;
           soff[i][0] = swz_offset(r, 2 * seg);
           soff[i][1] = swz_offset(r, 2 * seg + 1);
         }
-        const uint8_t* k8 = a.k8 + seg * 16;
-        const uint8_t* v8 = a.v8 + seg * 16;
-        auto fetch = [&](uint4 (&buf)[kGPW], const uint8_t* src, int rows) {
+        auto convert = [&](int it) {
+          uint8_t* stage = ring + (it % NS) * L::kStageBytes;
+          uint4 raw[kGPW];
 #pragma unroll
-          for (int i = 0; i < kGPW; ++i) {
-            const int rg = pw + kProducers * i;
-            const int row = __shfl_sync(0xffffffffu, rows, i * kRPI + sub);
-            buf[i] = rg < kRG ? ld_global_nc16(src + static_cast<size_t>(row) * D)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          }
-        };
-        auto put = [&](int it, const uint4 (&buf)[kGPW]) -> bool {
-          const int st = it % NS;
-          if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
-          uint8_t* stage = ring + st * L::kStageBytes;
+          for (int i = 0; i < kGPW; ++i)
+            if (pw + kProducers * i < kRG) raw[i] = ld_shared16(stage + stoff[i]);
+          __syncwarp();
 #pragma unroll
           for (int i = 0; i < kGPW; ++i) {
             if (pw + kProducers * i < kRG) {
               uint4 lo, hi;
-              e4m3x4_to_f16x4(buf[i].x, lo.x, lo.y);
-              e4m3x4_to_f16x4(buf[i].y, lo.z, lo.w);
-              e4m3x4_to_f16x4(buf[i].z, hi.x, hi.y);
-              e4m3x4_to_f16x4(buf[i].w, hi.z, hi.w);
+              e4m3x4_to_f16x4(raw[i].x, lo.x, lo.y);
+              e4m3x4_to_f16x4(raw[i].y, lo.z, lo.w);
+              e4m3x4_to_f16x4(raw[i].z, hi.x, hi.y);
+              e4m3x4_to_f16x4(raw[i].w, hi.z, hi.w);
               st_shared16(stage + soff[i][0], lo);
               st_shared16(stage + soff[i][1], hi);
             }
           }
           fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
-          mbar_arrive(full + st);
+          mbar_arrive(full + it % NS);
+        };
+        int pend0 = -1, pend1 = -1;  // items copied, not yet converted (oldest first)
+        auto copy8 = [&](int it, const uint8_t* src, int rows) -> bool {
+          const int st = it % NS;
+          if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
+          uint8_t* stage = ring + st * L::kStageBytes;
+#pragma unroll
+          for (int i = 0; i < kGPW; ++i) {
+            const int rg = pw + kProducers * i;
+            const int row = __shfl_sync(0xffffffffu, rows, i * kRPI + sub);
+            if (rg < kRG) cp_async16(stage + stoff[i], src + static_cast<size_t>(row) * D + seg * 16);
+          }
+          cp_async_commit();
           ++issued;
+          static_assert(kLag == 2, "the pending list holds two items");
+          if (pend1 >= 0) {
+            cp_async_wait_group<kLag>();  // the oldest pending item has landed
+            convert(pend0);
+            pend0 = pend1;
+            pend1 = it;
+          } else if (pend0 >= 0) {
+            pend1 = it;
+          } else {
+            pend0 = it;
+          }
           return true;
         };
         int bits;  // group bits: paired mode only
@@ -477,43 +498,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           r1[0] = load_rows(0, 1, &bits);
           r1[1] = load_rows(1, 1, &bits);
         }
-        uint4 bufA[kGPW], bufB[kGPW];
-        fetch(bufA, k8, r0[0]);
-        fetch(bufB, k8, r0[1]);
-        bool ok = put(k_item(0, 0), bufA);
-        fetch(bufA, v8, r0[0]);
-        ok = ok && put(k_item(1, 0), bufB);
+        bool ok = copy8(k_item(0, 0), a.k8, r0[0]) && copy8(k_item(1, 0), a.k8, r0[1]);
         for (int j = 0; ok && j < nkv; ++j) {
           if (a.fault && j >= 1) break;  // test-only: starve the MMA warp
           const bool more = j + 1 < nkv;
-          // indices of tile j+2, a step before their first use
+          for (int x = 0; ok && x < 2; ++x)
+            ok = copy8(v_item(x, j), a.v8, r0[x]) &&
+                 (!more || copy8(k_item(x, j + 1), a.k8, r1[x]));
           if (j + 2 < nkv) {
             r2[0] = load_rows(0, j + 2, &bits);
             r2[1] = load_rows(1, j + 2, &bits);
-          }
-          if (more) {
-            fetch(bufB, k8, r1[0]);                    // K_a(j+1)
-            ok = put(v_item(0, j), bufA);                // V_a(j)
-            if (ok) {
-              fetch(bufA, v8, r0[1]);                  // V_b(j)
-              ok = put(k_item(0, j + 1), bufB);          // K_a(j+1)
-            }
-            if (ok) {
-              fetch(bufB, k8, r1[1]);                  // K_b(j+1)
-              ok = put(v_item(1, j), bufA);              // V_b(j)
-            }
-            if (ok) {
-              fetch(bufA, v8, r1[0]);                  // V_a(j+1)
-              ok = put(k_item(1, j + 1), bufB);          // K_b(j+1)
-            }
-          } else {
-            fetch(bufB, v8, r0[1]);                    // V_b(j)
-            ok = put(v_item(0, j), bufA) && put(v_item(1, j), bufB);
           }
           r0[0] = r1[0];
           r0[1] = r1[1];
           r1[0] = r2[0];
           r1[1] = r2[1];
+        }
+        cp_async_wait_group<0>();
+        if (ok && !a.fault) {  // the last items
+          if (pend0 >= 0) convert(pend0);
+          if (pend1 >= 0) convert(pend1);
         }
       } else {
       // rows (and paired-mode group bits) of tiles j (V_x(j)), j+1 (K_x(j+1))

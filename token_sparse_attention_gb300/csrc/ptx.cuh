@@ -163,6 +163,25 @@ __device__ __forceinline__ uint4 ld_global_nc16(const void* src) {
   return v;
 }
 
+__device__ __forceinline__ uint4 ld_shared16(const void* src) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(src))
+               : "memory");
+  return v;
+}
+
+// Close this thread's current group of cp.async copies / wait until at most
+// N of its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void st_shared16(void* dst, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(dst)), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)
