@@ -54,7 +54,7 @@ TRAFFIC = {
     # --heads 4 --steps 1 --warmup 1 --no-e2e --no-cpu-baseline
     # --no-workloads --no-e4m3`), times 10 for the 40-head launch: heads are independent
     # and the grid scales with them
-    "attn.cu": {"sha": "22cdfa540c04", "bytes_per_launch": 7308997120},
+    "attn.cu": {"sha": "a02022ef129b", "bytes_per_launch": 7307924480},
 }
 
 

@@ -433,7 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // in one warp, so a __syncwarp between the reads and the writes
         // orders them.  The copies need no registers and run ahead like the
         // bf16 gathers; the conversion waits kLag items behind them.
-        constexpr int kLag = 2;
+        // the release a copy waits for needs every item up to kLag + 2
+        // before it converted: kLag <= NS - 2.  Converting one item behind
+        // the copies measured fastest (lags of 2 and 3 delay the stages the
+        // MMA is about to need).
+        constexpr int kLag = 1;
+        static_assert(kLag <= NS - 2, "conversions must not wait on the releases they gate");
         int stoff[kGPW], soff[kGPW][2];
 #pragma unroll
         for (int i = 0; i < kGPW; ++i) {
@@ -464,7 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();  // generic writes -> tensor-core operand reads
           mbar_arrive(full + it % NS);
         };
-        int pend0 = -1, pend1 = -1;  // items copied, not yet converted (oldest first)
+        int pend[kLag];  // items copied, not yet converted (oldest first; -1: none)
+#pragma unroll
+        for (int l = 0; l < kLag; ++l) pend[l] = -1;
         auto copy8 = [&](int it, const uint8_t* src, int rows) -> bool {
           const int st = it % NS;
           if (it >= NS && !wait_batch(release_batch(it - NS))) return false;
@@ -477,16 +484,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           cp_async_commit();
           ++issued;
-          static_assert(kLag == 2, "the pending list holds two items");
-          if (pend1 >= 0) {
+          if (pend[kLag - 1] >= 0) {
             cp_async_wait_group<kLag>();  // the oldest pending item has landed
-            convert(pend0);
-            pend0 = pend1;
-            pend1 = it;
-          } else if (pend0 >= 0) {
-            pend1 = it;
+            convert(pend[0]);
+#pragma unroll
+            for (int l = 0; l + 1 < kLag; ++l) pend[l] = pend[l + 1];
+            pend[kLag - 1] = it;
           } else {
-            pend0 = it;
+            bool placed = false;
+#pragma unroll
+            for (int l = 0; l < kLag; ++l)
+              if (!placed && pend[l] < 0) {
+                pend[l] = it;
+                placed = true;
+              }
           }
           return true;
         };
@@ -516,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_wait_group<0>();
         if (ok && !a.fault) {  // the last items
-          if (pend0 >= 0) convert(pend0);
-          if (pend1 >= 0) convert(pend1);
+#pragma unroll
+          for (int l = 0; l < kLag; ++l)
+            if (pend[l] >= 0) convert(pend[l]);
         }
       } else {
       // rows (and paired-mode group bits) of tiles j (V_x(j)), j+1 (K_x(j+1))
